@@ -1,0 +1,90 @@
+"""Planted mistakes: each mutant of the oracle source must fail at least one pin.
+
+A mutant is oracle.c with one plausible slip written in (a wrong head map, a
+dropped scale, a floor turned into a ceiling, the V half read as K, ...).  It
+is compiled to a temporary library on the CPU and the pins of
+test_oracle_pins.py are run against it; the test passes only when some pin
+catches the slip.  The oracle itself is never modified.
+"""
+import ctypes
+import os
+import subprocess
+import tempfile
+
+import pytest
+
+import oracle
+from tests import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+MUTANTS = {
+    "gqa head map modulo": ("const int hk = h / G;\n            const long L", "const int hk = h % Hkv;\n            const long L"),
+    "k_scale dropped": ("const double bmm1 = scale * q_scale * k_scale;", "const double bmm1 = scale * q_scale;"),
+    "v_scale dropped": ("const double bmm2 = v_scale;", "const double bmm2 = 1.0;"),
+    "window start ceil": ("long sp = orc_floor_div(L - span, P);", "long sp = orc_floor_div(L - span + P - 1, P);"),
+    "window span off by one": ("long span = window + sq - 1;", "long span = window + sq;"),
+    "V read from the K half": ("* 2L * D + D);", "* 2L * D);"),
+    "slot from the wrong token": ("long page = block_table[(long)b * bt_stride + j / P];\n                    if (page < 0 || page >= num_pages) {",
+                                  "long page = block_table[(long)b * bt_stride + (j + 1) / P];\n                    if (page < 0 || page >= num_pages) {"),
+    "lse in base 2": ("*lse_out = m + log(sum);", "*lse_out = m + log2(sum);"),
+    "segment prior dropped": ("denom += exp(l[g] + prior - mx);", "denom += exp(l[g] - mx);"),
+    "dead segment kept": ("if (used[(long)i * groups + g] <= 0) continue;\n                    double prior = g < topk ? bias[(long)i * topk + g] : 0.0;\n                    acc",
+                          "double prior = g < topk ? bias[(long)i * topk + g] : 0.0;\n                    acc"),
+    "local segment offset": (": (long)topk * bs);", ": (long)topk * bs + 1);"),
+    "merge ignores live mask": ("if (live && live[nn * S + s] <= 0) continue;\n                    double lg = part_lse[(nn * S + s) * H + h] + (prior ? prior[nn * S + s] : 0.0);\n                    if (lg == -INFINITY) continue;\n                    acc",
+                                "double lg = part_lse[(nn * S + s) * H + h] + (prior ? prior[nn * S + s] : 0.0);\n                    if (lg == -INFINITY) continue;\n                    acc"),
+    "bf16 decoded as low half": ("uint32_t u = ((uint32_t)h) << 16;", "uint32_t u = ((uint32_t)h) << 15;"),
+    "e4m3 exponent bias 8": ("v = ldexp((double)(8 + m), e - 10);", "v = ldexp((double)(8 + m), e - 11);"),
+    "causal position off by one": ("long pos = L - sq + i;", "long pos = L - sq + i - 1;"),
+}
+
+PINS = [
+    pins.test_decode_bf16_all_codes_match_torch,
+    pins.test_decode_e4m3_all_codes_match_torch,
+    pins.test_window_start_matches_hand_worked_rows,
+    pins.test_two_key_worked_example,
+    pins.test_lse_merge_worked_example,
+    pins.test_single_key_returns_its_value,
+    pins.test_zero_query_gives_log_count_and_mean,
+    pins.test_gqa_equals_mha_with_repeated_heads,
+    pins.test_fp8_power_of_two_scales_equal_bf16_on_dequantised_values,
+    pins.test_tiny_workload_matches_brute_force,
+    pins.test_segments_match_brute_force,
+    pins.test_segments_combine_equals_union_attention_with_bias,
+    pins.test_lse_merge_dead_parts_and_all_dead,
+    lambda: pins.test_paged_decode_matches_brute_force(dict(sq=3, causal=True, window=10)),
+    lambda: pins.test_paged_decode_matches_brute_force(dict(sq=3, window=20)),
+]
+
+
+def _compile(src_text, out_path):
+    with tempfile.NamedTemporaryFile("w", suffix=".c", delete=False) as f:
+        f.write(src_text)
+        c_path = f.name
+    try:
+        subprocess.run(["gcc", "-O1", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", c_path,
+                        "-o", out_path, "-lm"], check=True, capture_output=True)
+    finally:
+        os.unlink(c_path)
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) >= 1, f"mutation site for {name!r} not found in oracle.c"
+    so = str(tmp_path / "mutant.so")
+    _compile(src.replace(old, new, 1), so)
+    saved = oracle._load()
+    try:
+        oracle._lib = oracle._bind(ctypes.CDLL(so))
+        caught = []
+        for pin in PINS:
+            try:
+                pin()
+            except (AssertionError, ValueError):
+                caught.append(getattr(pin, "__name__", "lambda"))
+        assert caught, f"no pin caught mutant {name!r}"
+    finally:
+        oracle._lib = saved
