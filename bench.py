@@ -1,0 +1,388 @@
+"""Benchmark: paged-decode KV bandwidth on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+A step is one paged_decode call over the workload's whole batch (window
+restriction, page gather, logits, online softmax, P.V, Split-KV merge and
+epilogue, all in one kernel launch).  Inputs are resident in HBM; the L2 is
+flushed (a 512 MiB write) before every timed step and the KV stream is larger
+than the L2 anyway.  Each step is timed with CUDA events on the launching
+stream; value = algorithmic KV bytes of all ranks / max over ranks of the
+summed step time.  One JSON line is printed by rank 0.
+
+--impl reference times the fp64 CPU oracle on the host cores instead, on a
+bounded sample of the same workload per step, in the same metric.
+
+Under torchrun (N > 1) each rank runs an independent replica of the workload
+on its own GPU (the path has no exchange step): weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import datetime as _dt
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode KV GB/s and % of GB300 HBM peak; µs/call at B=64 bf16 decode"
+DEFAULT_WORKLOAD = "gqa_decode_b64"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 512 << 20
+
+
+# ------------------------------------------------------------- accounting
+def visible_keys(case) -> np.ndarray:
+    """Keys each request reads (page-aligned window start, as the kernel sees them)."""
+    L = case.seq_lens.astype(np.int64)
+    if case.window > 0 and not case.causal:
+        start = np.maximum(0, (L - (case.window + case.sq - 1)) // case.page_size) * case.page_size
+    elif case.window > 0:
+        start = np.maximum(0, L - case.sq - case.window + 1)
+    else:
+        start = np.zeros_like(L)
+    return np.maximum(L - start, 0)
+
+
+def algorithmic_bytes(case) -> dict:
+    """Bytes a perfect kernel must move: visible K and V rows, q, out, lse,
+    the block-table entries of the visible pages and seq_lens."""
+    elt = 1 if case.dtype == "fp8" else 2
+    vis = visible_keys(case)
+    kv = int(vis.sum()) * case.num_kv_heads * 2 * case.head_dim * elt
+    B, sq, Hq, D = case.q.shape
+    q = case.q.nbytes
+    out = B * sq * Hq * D * 2
+    lse = B * sq * Hq * 4
+    table = int(np.ceil(vis / case.page_size).sum()) * 4
+    return {"kv": kv, "total": kv + q + out + lse + table + B * 4}
+
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
+
+
+def source_digest() -> str:
+    """sha256 over the kernel sources: a traffic figure is valid only for this digest."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_decode_15_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """dram bytes per launch from the committed ncu summary, if it matches these sources."""
+    path = os.path.join(ROOT, "profiles", f"decode_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    t = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    d = re.search(r"source_digest:\s*([0-9a-f]+)", text)
+    if not t or not d or d.group(1) != source_digest():
+        return None
+    return int(t.group(1))
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.proc = None
+        self.index = index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self, t0: float, t1: float) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                ts = _dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
+        if not inside and rows:
+            inside = [min(rows, key=lambda r: abs(r[0] - t1))]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in inside for n, v in zip(names, r[3]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside)}
+
+
+# ------------------------------------------------------------ device side
+def _device_inputs(case, torch):
+    import paged_kv_decode_15_gb300 as pkd
+    from workloads import to_torch
+    q = to_torch(case.q, case.dtype)
+    cache = to_torch(case.kv_cache, case.dtype)
+    bt = to_torch(case.block_table, "int32")
+    lens = to_torch(case.seq_lens, "int32")
+    out = torch.empty(case.q.shape, dtype=torch.bfloat16 if case.dtype != "fp16" else torch.float16, device="cuda")
+    lse = torch.empty(case.q.shape[:3], dtype=torch.float32, device="cuda")
+    max_kv_len = int(case.block_table.shape[1] * case.page_size)
+    kv_code = {"bf16": pkd.BF16, "fp16": pkd.FP16, "fp8": pkd.FP8_E4M3}[case.dtype]
+    flags = pkd.FLAG_CAUSAL if case.causal else 0
+    ws = torch.empty(pkd.workspace_size(case.batch, case.sq, case.num_heads, case.num_kv_heads, case.head_dim,
+                                        case.page_size, max_kv_len, kv_code, case.window, 0, flags),
+                     dtype=torch.uint8, device="cuda")
+    pkd.workspace_init(ws)
+    return dict(q=q, cache=cache, bt=bt, lens=lens, out=out, lse=lse, ws=ws, max_kv_len=max_kv_len)
+
+
+def _call(case, d, pkd, q=None, bt=None, lens=None):
+    pkd.paged_decode(q if q is not None else d["q"], d["cache"], bt if bt is not None else d["bt"],
+                     lens if lens is not None else d["lens"], case.scale, case.window, out=d["out"],
+                     lse=d["lse"], q_scale=case.q_scale, k_scale=case.k_scale, v_scale=case.v_scale,
+                     max_kv_len=d["max_kv_len"], workspace=d["ws"], causal=case.causal)
+
+
+def run_gpu(args, rank, world, dist):
+    import torch
+    import paged_kv_decode_15_gb300 as pkd
+    import workloads as wl
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+    pkd.build()
+    pkd.load_library()
+    case = wl.WORKLOADS[args.workload]()
+    acct = algorithmic_bytes(case)
+    d = _device_inputs(case, torch)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        _call(case, d, pkd)
+    torch.cuda.synchronize()
+    if pkd.workspace_check(d["ws"]) != pkd.OK:
+        raise RuntimeError("device status word set during warm-up: " + pkd.load_library().pkd_last_error().decode())
+
+    sampler = ClockSampler(torch.cuda.current_device())
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        _call(case, d, pkd)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop(t0, t1)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = float(sum(step_ms))
+
+    # end to end through the public call: pinned host inputs in, results out
+    qh = torch.empty(d["q"].shape, dtype=d["q"].dtype, pin_memory=True).copy_(d["q"].cpu())
+    bth = torch.empty(d["bt"].shape, dtype=torch.int32, pin_memory=True).copy_(d["bt"].cpu())
+    lensh = torch.empty(d["lens"].shape, dtype=torch.int32, pin_memory=True).copy_(d["lens"].cpu())
+    outh = torch.empty(d["out"].shape, dtype=d["out"].dtype, pin_memory=True)
+    lseh = torch.empty(d["lse"].shape, dtype=torch.float32, pin_memory=True)
+    h2d = qh.nbytes + bth.nbytes + lensh.nbytes
+    d2h = outh.nbytes + lseh.nbytes
+    e2e_steps = args.steps
+    es = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    ee = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    torch.cuda.synchronize()
+    for i in range(e2e_steps):
+        flush.zero_()
+        es[i].record(stream)
+        d["q"].copy_(qh, non_blocking=True)
+        d["bt"].copy_(bth, non_blocking=True)
+        d["lens"].copy_(lensh, non_blocking=True)
+        _call(case, d, pkd)
+        outh.copy_(d["out"], non_blocking=True)
+        lseh.copy_(d["lse"], non_blocking=True)
+        ee[i].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = float(sum(s.elapsed_time(e) for s, e in zip(es, ee)))
+    status = pkd.workspace_check(d["ws"])
+    if status != pkd.OK:
+        raise RuntimeError("device status word set: " + pkd.load_library().pkd_last_error().decode())
+
+    if dist:
+        import torch.distributed as tdist
+        t = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device="cuda")
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        total_ms, e2e_ms = float(t[0]), float(t[1])
+    return case, acct, step_ms, total_ms, e2e_ms, h2d, d2h, clocks
+
+
+def cpu_baseline(case, budget_s: float = 12.0) -> dict:
+    """Time the oracle, as it stands, on a bounded sample of the workload's requests."""
+    import oracle
+    threads = os.cpu_count() or 1
+    order = np.random.default_rng(0).permutation(case.batch)
+    n = 1
+    t = _time_oracle(case, order[:1], threads)
+    n = int(min(case.batch, max(1, budget_s / max(t, 1e-6))))
+    if n > 1:
+        t = _time_oracle(case, order[:n], threads)
+    sub = _subcase(case, order[:n])
+    gbs = algorithmic_bytes(sub)["kv"] / t / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} of {case.batch} requests (all heads), fp64 C oracle with OpenMP over "
+                      f"(request, head), {t:.2f} s"}
+
+
+def _subcase(case, idx):
+    import copy
+    sub = copy.copy(case)
+    sub.q = case.q[idx]
+    sub.block_table = case.block_table[idx]
+    sub.seq_lens = case.seq_lens[idx]
+    return sub
+
+
+def _time_oracle(case, idx, threads):
+    import oracle
+    sub = _subcase(case, idx)
+    t = time.perf_counter()
+    oracle.paged_decode(sub.q, sub.dtype, sub.kv_cache, sub.dtype, sub.block_table, sub.seq_lens,
+                        threads=threads, **sub.oracle_kwargs())
+    return time.perf_counter() - t
+
+
+def run_reference(args, rank):
+    """The oracle arm: each step is a bounded sample of the workload on the host cores."""
+    import oracle
+    import workloads as wl
+    oracle.build()
+    case = wl.WORKLOADS[args.workload]()
+    threads = os.cpu_count() or 1
+    order = np.random.default_rng(0).permutation(case.batch)
+    t1 = _time_oracle(case, order[:1], threads)
+    per_step_budget = max(0.02, 120.0 / max(1, args.steps + args.warmup))
+    n = int(min(case.batch, max(1, per_step_budget / max(t1, 1e-6))))
+    sub = _subcase(case, order[:n])
+    for _ in range(args.warmup):
+        _time_oracle(case, order[:n], threads)
+    total = 0.0
+    for _ in range(args.steps):
+        total += _time_oracle(case, order[:n], threads)
+    kv = algorithmic_bytes(sub)["kv"]
+    value = kv * args.steps / total / 1e9
+    cfg = workload_config(case, args)
+    sample = f"{n} of {case.batch} requests per step (all heads), fp64 C oracle, OpenMP over (request, head)"
+    return {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
+            "impl": "reference",
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def workload_config(case, args) -> dict:
+    return {"workload": case.name, "batch": case.batch, "sq": case.sq, "num_heads": case.num_heads,
+            "num_kv_heads": case.num_kv_heads, "head_dim": case.head_dim, "page_size": case.page_size,
+            "kv_dtype": case.dtype, "window": case.window, "causal": case.causal,
+            "seq_lens": {"min": int(case.seq_lens.min()), "max": int(case.seq_lens.max()),
+                         "total": int(case.seq_lens.sum())},
+            "pool_pages": case.num_pages, "l2": "L2 flushed (512 MiB write) before every timed step; "
+                                                "KV stream larger than L2",
+            "parallelism": f"replicas{args.gpus}" if args.gpus > 1 else "single"}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="pkd", choices=["pkd", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, rank)), flush=True)
+        return
+
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group(backend="nccl")
+        dist = tdist
+    case, acct, step_ms, total_ms, e2e_ms, h2d, d2h, clocks = run_gpu(args, rank, world, dist)
+    if rank == 0:
+        peaks = load_peaks()
+        steps = args.steps
+        gbs = acct["kv"] * world * steps / (total_ms / 1e3) / 1e9
+        avg_ms = total_ms / steps
+        achieved = acct["total"] / (avg_ms / 1e3) / 1e9
+        traffic = profiled_traffic(case.name)
+        line = {
+            "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": round(avg_ms, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": case.dtype, "data": "synthetic", "config": workload_config(case, args),
+            "us_per_call": round(avg_ms * 1e3, 2), "us_per_call_median": round(statistics.median(step_ms) * 1e3, 2),
+            "pct_of_hbm_peak": round(100 * gbs / world / peaks["hbm_gbs"], 2),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+                         "algorithmic_bytes_per_launch": acct["total"], "peak_source": peaks["source"],
+                         "kernel": "paged decode (one launch per step)"},
+            "e2e": {"value": round(acct["kv"] * world * steps / (e2e_ms / 1e3) / 1e9, 2), "unit": "GB/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "us_per_call": round(e2e_ms / steps * 1e3, 2),
+                    "note": "q, block_table, seq_lens in from pinned host memory, out and lse back, every step; "
+                            "the KV cache is resident device state"},
+            "gpu_launches": steps,
+            "clocks": clocks,
+        }
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(case)
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

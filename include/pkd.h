@@ -1,0 +1,186 @@
+/*
+ * pkd -- attention over a paged KV cache on GB300 (sm_103a).
+ *
+ * C ABI.  Every pointer named "device" is a CUDA device address owned by the
+ * caller; the library never allocates, frees or synchronises on its own (the
+ * one exception is pkd_workspace_check, which reads a status word back).
+ * Calls are asynchronous on the stream passed as `stream` (a cudaStream_t;
+ * NULL is the legacy default stream).  All functions are thread-safe; the
+ * message of the last failure is kept per host thread (pkd_last_error).
+ *
+ * Sources of the operations (vLLM API pages, by title and section):
+ *   [TS]   vllm.v1.attention.backends.flashinfer_ts -- module docstring
+ *          ("Layout", "Sliding window"), FlashInferTSImpl.forward,
+ *          FlashInferTSImpl._kv_views, FlashInferTSMetadataBuilder.build,
+ *          ._restrict_to_window, ._get_plan, _kv_kernel_dtype.
+ *   [DASH] vllm.v1.attention.ops.dash_attention -- flash_dash_attention.
+ *   [FA]   vllm.v1.attention.backends.fa_utils --
+ *          FlashAttentionCuTeDSLCompileSpec (Split-KV, return_softmax_lse).
+ */
+#ifndef PKD_H_
+#define PKD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PKD_OK = 0,
+    PKD_EINVAL = 1,          /* bad pointer, size, stride or alignment */
+    PKD_EUNSUPPORTED = 2,    /* valid request outside what the kernels implement */
+    PKD_ECUDA = 3,           /* a CUDA runtime/driver call failed (message has the CUDA error) */
+    PKD_EDEVICE_BOUNDS = 4,  /* a kernel met an out-of-range page or length (see pkd_workspace_check) */
+    PKD_ETIMEOUT = 5         /* a kernel gave up waiting on one of its own copies */
+} pkd_status;
+
+typedef enum {
+    PKD_BF16 = 0,
+    PKD_FP16 = 1,
+    PKD_FP8_E4M3 = 2,        /* e4m3 "fn": uint8 storage, no infinities [TS _kv_kernel_dtype] */
+    PKD_FP32 = 3
+} pkd_dtype;
+
+/* Flags for pkd_paged_decode. */
+#define PKD_FLAG_CAUSAL 1u      /* causal mask inside the query block, exact per-token window */
+#define PKD_FLAG_MMA_SMALL_M 2u /* use the tensor-core kernel even when sq*Hq/Hkv < 16 */
+#define PKD_FLAG_FMA 4u         /* force the CUDA-core kernel (only when sq*Hq/Hkv <= 8) */
+
+/* Library version, major*10000 + minor*100 + patch. */
+int pkd_version(void);
+
+/* Message of the last non-OK status returned on this host thread ("" if none). */
+const char* pkd_last_error(void);
+
+/*
+ * Bytes of workspace pkd_paged_decode needs for a plan.  The plan is fixed by
+ * the shapes and by max_kv_len, an upper bound on every seq_lens entry (the
+ * constant K/V capacity of [TS FlashInferTSMetadataBuilder._max_kv_len]), so
+ * one workspace serves every call with the same shapes, e.g. every replay of
+ * a captured CUDA graph.  chunk_tokens is the Split-KV chunk (0 = automatic;
+ * otherwise a multiple of page_size).  flags as for pkd_paged_decode.
+ * Returns 0 for an invalid request (the reason is in pkd_last_error).
+ */
+size_t pkd_paged_decode_workspace_size(int batch, int sq, int num_heads, int num_kv_heads,
+                                       int head_dim, int page_size, int max_kv_len,
+                                       pkd_dtype kv_dtype, int window, int chunk_tokens,
+                                       unsigned flags);
+
+/*
+ * Zero a workspace (asynchronously on `stream`).  Needed once, before its
+ * first use: every later call leaves the workspace ready for the next one.
+ */
+pkd_status pkd_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronise `stream`, read the workspace's status word and clear it.
+ * Returns PKD_OK, PKD_EDEVICE_BOUNDS (a seq_lens entry above max_kv_len or
+ * below 0, or a block-table entry outside [0, num_pages): the kernel skipped
+ * those keys) or PKD_ETIMEOUT.  The kernels never trap.
+ */
+pkd_status pkd_workspace_check(void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Paged decode: attention of a uniform query block per request over that
+ * request's keys in a paged cache [TS FlashInferTSImpl.forward].
+ *
+ *   q            device, [batch, sq, num_heads, head_dim] contiguous, q_dtype
+ *   kv_cache     device, [num_pages, num_kv_heads, page_size, 2*head_dim]
+ *                contiguous, kv_dtype.  K = [..., :head_dim], V = [..., head_dim:]
+ *                (token stride 2*head_dim [TS _kv_views, "Layout"]); 16-byte aligned.
+ *   block_table  device int32 [batch, block_table_stride]: token t of request b
+ *                lives in page block_table[b, t / page_size], slot t % page_size.
+ *                Columns past a request's last page are never read.
+ *   seq_lens     device int32 [batch], each in [0, max_kv_len].
+ *   out          device, [batch, sq, num_heads, head_dim], out_dtype (bf16, fp16, fp32)
+ *   lse          device fp32 [batch, sq, num_heads] natural-log LSE, or NULL
+ *   workspace    device, >= pkd_paged_decode_workspace_size(...) bytes,
+ *                zeroed once by pkd_workspace_init; 256-byte aligned.
+ *
+ * Query head h reads KV head h / (num_heads / num_kv_heads).  Logits are
+ * (scale * q_scale * k_scale) * q.k and the output is scaled by v_scale
+ * (bmm1 / bmm2 of [TS forward]); for fp8 caches q is already fp8 with
+ * scale q_scale (q_dtype must equal kv_dtype).
+ *
+ * Masks.  Without PKD_FLAG_CAUSAL every query token of the block sees every
+ * visible key ("dense", [TS module docstring]).  window > 0 restricts the
+ * visible keys to the page-aligned suffix of [TS _restrict_to_window]:
+ *   start_page = max(0, floor((L - (window + sq - 1)) / page_size)),
+ * keys [start_page * page_size, L), one start for the whole block.  With
+ * PKD_FLAG_CAUSAL query token i (position L - sq + i) sees keys up to its
+ * position and, when window > 0, from position - (window - 1) on
+ * ([TS _get_plan] mask_type "causal", window_left = window - 1).
+ * A query row with no visible key gets out = 0 and lse = -inf.
+ *
+ * Long sequences are split into chunks of chunk_tokens keys whose partial
+ * results are merged by LSE inside the same launch [FA num_splits].
+ *
+ * Limits: head_dim 64 or 128; page_size a multiple of 16; num_heads a
+ * multiple of num_kv_heads; sq * num_heads / num_kv_heads <= 64 (<= 8 for fp8);
+ * fp8 caches need head_dim 128.  Anything else: PKD_EUNSUPPORTED.
+ */
+pkd_status pkd_paged_decode(const void* q, pkd_dtype q_dtype,
+                            const void* kv_cache, pkd_dtype kv_dtype, int64_t num_pages,
+                            const int32_t* block_table, int64_t block_table_stride,
+                            const int32_t* seq_lens,
+                            int batch, int sq, int num_heads, int num_kv_heads, int head_dim,
+                            int page_size, int max_kv_len,
+                            float scale, float q_scale, float k_scale, float v_scale, int window,
+                            void* out, pkd_dtype out_dtype, float* lse,
+                            void* workspace, size_t workspace_bytes, int chunk_tokens,
+                            unsigned flags, void* stream);
+
+/*
+ * DASH segmented attention with its combine [DASH flash_dash_attention].
+ *
+ *   q        device [n, num_heads, head_dim], dtype (bf16 or fp16)
+ *   k, v     device [n * (topk*bs + local), num_kv_heads, head_dim], dtype, contiguous
+ *   used     device int32 [n * (topk + 1)]: valid prefix length of each segment;
+ *            query i's segment g < topk starts at row i*(topk*bs+local) + g*bs
+ *            (capacity bs), its local segment at i*(topk*bs+local) + topk*bs
+ *            (capacity local).  Values are clamped to [0, capacity].
+ *   bias     device fp32 [n, topk] prior of each gathered segment (the local
+ *            segment's prior is 0); may be NULL when topk == 0.
+ *   out      device [n, num_heads, head_dim], dtype
+ *   seg_out  device fp32 [n, topk+1, num_heads, head_dim] per-segment outputs, or NULL
+ *   seg_lse  device fp32 [n, topk+1, num_heads] per-segment natural-log LSE, or NULL
+ *
+ * Each (query, segment, head) is softmax attention over the segment's used
+ * rows with scale head_dim^-0.5, giving (o_g, lse_g); an empty segment gives
+ * (0, -inf).  out = sum_g w_g o_g with w = softmax over live segments
+ * (used > 0) of lse_g + prior_g; a query with no live segment gets 0.
+ * Limits: head_dim 64 or 128, bs and local multiples of 8, num_heads a
+ * multiple of num_kv_heads with num_heads / num_kv_heads <= 16.
+ */
+pkd_status pkd_segmented_attention(const void* q, const void* k, const void* v, pkd_dtype dtype,
+                                   const int32_t* used, const float* bias,
+                                   int n, int num_heads, int num_kv_heads, int head_dim,
+                                   int topk, int bs, int local,
+                                   void* out, float* seg_out, float* seg_lse, void* stream);
+
+/*
+ * LSE merge of partial attention results: the Split-KV merge [FA] and, with a
+ * prior and a live mask, the segment combine [DASH flash_dash_attention].
+ *
+ *   part_out  device fp32 [n, parts, heads, head_dim]
+ *   part_lse  device fp32 [n, parts, heads] natural-log LSE of each part
+ *   prior     device fp32 [n, parts] added to each part's LSE, or NULL
+ *   live      device int32 [n, parts]; part p of row n is dead when <= 0, or NULL
+ *   out       device [n, heads, head_dim], out_dtype (bf16, fp16, fp32)
+ *   lse_out   device fp32 [n, heads] = ln sum_{live p} exp(lse_p + prior_p), or NULL
+ *
+ * out = sum over live parts of exp(lse_p + prior_p - lse_out) * part_out_p;
+ * a dead part (or one with lse -inf) is never read; a row with no live part
+ * gets out = 0 and lse_out = -inf.  Limits: head_dim <= 256, parts <= 1024.
+ */
+pkd_status pkd_lse_merge(const float* part_out, const float* part_lse, const float* prior,
+                         const int32_t* live, int n, int parts, int heads, int head_dim,
+                         void* out, pkd_dtype out_dtype, float* lse_out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKD_H_ */

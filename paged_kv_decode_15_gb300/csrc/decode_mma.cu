@@ -1,0 +1,44 @@
+// Instantiations of the tensor-core decode kernel.
+#include "decode_mma.cuh"
+#include "launch.h"
+
+namespace pkd {
+
+constexpr int kMmaNbuf = 2;
+
+template <int D, bool kBF16, int MT, int NT>
+static cudaError_t launch_one(const CUtensorMap& tmap, const DecodeParams& p, dim3 grid, cudaStream_t stream) {
+    using S = MmaShape<D, MT, NT, kMmaNbuf>;
+    auto kern = decode_mma_kernel<D, kBF16, MT, NT, kMmaNbuf>;
+    static bool configured = false;  // benign race: the attribute call is idempotent
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    kern<<<grid, kNW * 32, S::SMEM, stream>>>(tmap, p);
+    return cudaGetLastError();
+}
+
+int decode_mma_smem(int D, int MT, int NT) {
+#define PKD_MMA_SMEM(d, mt, nt) \
+    if (D == d && MT == mt && NT == nt) return MmaShape<d, mt, nt, kMmaNbuf>::SMEM;
+    PKD_MMA_SMEM(128, 1, 1) PKD_MMA_SMEM(128, 1, 2) PKD_MMA_SMEM(128, 2, 3) PKD_MMA_SMEM(128, 2, 4)
+    PKD_MMA_SMEM(64, 1, 1) PKD_MMA_SMEM(64, 1, 2) PKD_MMA_SMEM(64, 2, 3) PKD_MMA_SMEM(64, 2, 4)
+#undef PKD_MMA_SMEM
+    return -1;
+}
+
+cudaError_t launch_decode_mma(int D, bool bf16, int MT, int NT, const CUtensorMap& tmap,
+                              const DecodeParams& p, dim3 grid, cudaStream_t stream) {
+#define PKD_MMA_CASE(d, mt, nt)                                                              \
+    if (D == d && MT == mt && NT == nt)                                                      \
+        return bf16 ? launch_one<d, true, mt, nt>(tmap, p, grid, stream)                     \
+                    : launch_one<d, false, mt, nt>(tmap, p, grid, stream);
+    PKD_MMA_CASE(128, 1, 1) PKD_MMA_CASE(128, 1, 2) PKD_MMA_CASE(128, 2, 3) PKD_MMA_CASE(128, 2, 4)
+    PKD_MMA_CASE(64, 1, 1) PKD_MMA_CASE(64, 1, 2) PKD_MMA_CASE(64, 2, 3) PKD_MMA_CASE(64, 2, 4)
+#undef PKD_MMA_CASE
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace pkd

@@ -1,0 +1,136 @@
+// Tensor-core paged decode (mma.sync m16n8k16, fp32 accumulate).
+//
+// The GQA group and the query block are folded into one M dimension of
+// M = sq * Hq/Hkv query rows per (request, kv head).  Per 16-key stage:
+//   S   = Q K^T     A = Q (M padded to 16-row tiles, fragments from shared
+//                   memory), B = K straight from the swizzled TMA stage
+//   P   = online-softmax(S) in fp32, rounded to the operand type
+//   O^T += V^T P^T  "swapped" so that M sits in the 8-wide N dimension: A = V^T
+//                   (ldmatrix.trans of the stage), B = P^T, which is exactly
+//                   the accumulator layout of S -- no shuffles between the
+//                   two products, and rows only pad to a multiple of 8.
+// Keys arrive through a per-warp ring of NBUF stages filled by 2-D TMA tile
+// loads (128-byte swizzle) addressed by the block table, so K and V are read
+// from the cache's own [pages, Hkv, P, 2*D] layout without any repacking.
+#pragma once
+
+#include "mma_warp.cuh"
+
+namespace pkd {
+
+template <int D, int MT, int NT, int NBUF>
+struct MmaShape {
+    static constexpr int ELT = 2;
+    static constexpr int ROWB = D * ELT;
+    static constexpr int KBOX = ROWB / 128;
+    static constexpr int HALF = KBOX * 2048;
+    static constexpr int STAGE = 2 * HALF;
+    static constexpr int MROWS = MT * 16;
+    static constexpr int QSTRIDE = D * 2 + 16;           // bytes per staged q row
+    static constexpr int OSTRIDE = D + 4;                // floats per merge row
+    static constexpr int RING = kNW * NBUF * STAGE;
+    static constexpr int MERGE = kNW * MROWS * OSTRIDE * 4;
+    static constexpr int BIG = RING > MERGE ? RING : MERGE;
+    static constexpr int OFF_BARS = BIG;
+    static constexpr int OFF_PAGES = OFF_BARS + kNW * NBUF * 8;
+    static constexpr int OFF_Q = OFF_PAGES + kMaxCtaPages * 4;
+    static constexpr int OFF_ML = OFF_Q + MROWS * QSTRIDE;
+    static constexpr int OFF_FLAG = OFF_ML + 2 * kNW * MROWS * 4;
+    static constexpr int SMEM = OFF_FLAG + 16 + 1024;    // + slack to align the base to 1 KiB
+};
+
+template <int D, bool kBF16, int MT, int NT, int NBUF>
+__global__ void __launch_bounds__(kNW * 32)
+decode_mma_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p) {
+    using S = MmaShape<D, MT, NT, NBUF>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::OFF_BARS);
+    int* pages = reinterpret_cast<int*>(smem + S::OFF_PAGES);
+    uint8_t* qs = smem + S::OFF_Q;
+    float* wm = reinterpret_cast<float*>(smem + S::OFF_ML);
+    float* wl = wm + kNW * S::MROWS;
+    int* flag = reinterpret_cast<int*>(smem + S::OFF_FLAG);
+
+    CtaWork w;
+    if (!cta_setup<D>(p, w)) return;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        prefetch_tmap(&tmap);
+        for (int i = 0; i < kNW * NBUF; ++i) mbar_init(smem_u32(bars + i), 1);
+        fence_barrier_init();
+    }
+    load_cta_pages(p, w, pages);
+
+    // stage the M query rows (zero padding rows) for ldmatrix
+    {
+        constexpr int VPR = D * 2 / 16;  // 16-byte vectors per row
+        const uint4* qg = reinterpret_cast<const uint4*>(p.q);
+        for (int e = tid; e < S::MROWS * VPR; e += blockDim.x) {
+            const int r = e / VPR, v = e % VPR;
+            uint4 val = make_uint4(0u, 0u, 0u, 0u);
+            if (r < p.M) {
+                const int i = r / p.G, g = r % p.G;
+                const long long row = (static_cast<long long>(w.b) * p.sq + i) * p.Hq + w.hk * p.G + g;
+                val = __ldg(qg + row * VPR + v);
+            }
+            *reinterpret_cast<uint4*>(qs + r * S::QSTRIDE + v * 16) = val;
+        }
+    }
+    __syncthreads();
+
+    const int nst = (w.t1 - w.t0 + kStageTok - 1) / kStageTok;
+    const int my_n = nst > warp ? (nst - warp + kNW - 1) / kNW : 0;
+    uint8_t* ring_gen = smem + warp * NBUF * S::STAGE;
+    const uint32_t ring = smem_u32(ring_gen);
+    const uint32_t bar0 = smem_u32(bars + warp * NBUF);
+    const uint64_t pol = policy_evict_first();
+    if (lane == 0)
+        for (int k = 0; k < NBUF && k < my_n; ++k)
+            issue_stage<D, 2>(&tmap, p, w, pages, warp + k * kNW, ring + k * S::STAGE, bar0 + 8 * k, pol);
+
+    MmaWarp<D, kBF16, MT, NT> wp;
+    wp.load_q(smem_u32(qs), S::QSTRIDE, lane);
+    wp.reset();
+    const int L = w.L;
+
+    int timed_out = 0, consumed = 0;
+    for (int k = 0; k < my_n; ++k) {
+        const int buf = k % NBUF;
+        if (!mbar_wait(bar0 + 8 * buf, (k / NBUF) & 1, p.status)) {
+            timed_out = 1;
+            break;
+        }
+        consumed = k + 1;
+        const int stage = warp + k * kNW;
+        const int tok0 = w.t0 + stage * kStageTok;
+        int nvalid = min(kStageTok, w.t1 - tok0);
+        if (pages[(tok0 - w.t0) / p.P] < 0) nvalid = 0;
+        const uint32_t st = ring + buf * S::STAGE;
+        if (nvalid < kStageTok) zero_tail_v<D, 2>(ring_gen + buf * S::STAGE, nvalid, lane);
+        wp.consume(st, S::HALF, nvalid, p.scale_log2, 0.f,
+                   [&](int row, int kt) { return row_sees(p, L, row, tok0 + kt); }, lane);
+        __syncwarp();
+        if (lane == 0 && k + NBUF < my_n) {
+            fence_proxy_async();
+            issue_stage<D, 2>(&tmap, p, w, pages, warp + (k + NBUF) * kNW, st, bar0 + 8 * buf, pol);
+        }
+    }
+    if (timed_out) {
+        // let this warp's other copies land before the CTA leaves or reuses the ring
+        if (lane == 0) raise_status(p, kErrTimeout);
+        for (int k = consumed + 1; k < my_n && k < consumed + NBUF; ++k)
+            mbar_wait(bar0 + 8 * (k % NBUF), (k / NBUF) & 1, p.status);
+    }
+
+    // ---- per-warp state to shared memory (the ring is reused for O)
+    wp.reduce_l();
+    __syncthreads();
+    float* O = reinterpret_cast<float*>(smem);
+    wp.store(O + warp * S::MROWS * S::OSTRIDE, wm + warp * S::MROWS, wl + warp * S::MROWS, S::OSTRIDE, lane);
+    __syncthreads();
+    cta_finish<D, S::OSTRIDE>(p, w, O, wm, wl, S::MROWS, flag);
+}
+
+}  // namespace pkd

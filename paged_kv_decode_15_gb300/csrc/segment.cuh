@@ -1,0 +1,34 @@
+// Parameters of the DASH segmented-attention and LSE-merge kernels.
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+namespace pkd {
+
+struct SegmentParams {
+    CUtensorMap kmap, vmap;   // 3-D maps over k, v: {head_dim, Hkv, rows}
+    const void* q;            // [n, Hq, D]
+    const int32_t* used;      // [n, topk+1]
+    const float* bias;        // [n, topk]
+    void* out;                // [n, Hq, D] (q dtype)
+    float* seg_out;           // [n, topk+1, Hq, D] or null
+    float* seg_lse;           // [n, topk+1, Hq] or null
+    int n, Hq, Hkv, G, D, topk, bs, local;
+    int bf16;
+    float scale_log2;         // D^-0.5 * log2(e)
+};
+
+struct MergeParams {
+    const float* part_out;    // [n, parts, heads, D]
+    const float* part_lse;    // [n, parts, heads], natural log
+    const float* prior;       // [n, prior_cols] or null; parts >= prior_cols get prior 0
+    const int32_t* live;      // [n, parts] or null
+    int n, parts, heads, D;
+    int prior_cols;
+    void* out;                // [n, heads, D]
+    int out_dtype;
+    float* lse_out;           // [n, heads] or null
+};
+
+}  // namespace pkd

@@ -1,0 +1,125 @@
+"""The C ABI boundary without a GPU: the library loads, exports every symbol the
+header declares, plans workspaces on the host, and rejects bad calls before
+any CUDA work (status codes and messages)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_decode_15_gb300 as pkd
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pkd.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pkd.build()
+    return pkd.load_library()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkd_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_symbols():
+    assert set(declared_symbols()) == set(pkd.SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_version(lib):
+    assert pkd.version() == 10000
+
+
+def test_workspace_plan_is_a_host_function(lib):
+    # gqa decode, B=64, Hq=32, Hkv=8, D=128, P=16, capacity 4096
+    n = pkd.workspace_size(64, 1, 32, 8, 128, 16, 4096, pkd.BF16)
+    assert n > 0 and n % 256 == 0
+    # more splits for longer capacity
+    assert pkd.workspace_size(8, 1, 64, 8, 128, 64, 131072, pkd.FP8_E4M3) > 0
+    # explicit chunk: 4096 / 256 = 16 splits -> partials [512 units, 16, 4 rows, 128] fp32 at least
+    m = pkd.workspace_size(64, 1, 32, 8, 128, 16, 4096, pkd.BF16, chunk_tokens=256)
+    assert m >= 512 * 16 * 4 * 128 * 4
+
+
+@pytest.mark.parametrize("args,needle", [
+    ((2, 1, 6, 4, 128, 16, 100, pkd.BF16), "multiple of num_kv_heads"),
+    ((2, 1, 8, 2, 96, 16, 100, pkd.BF16), "head_dim"),
+    ((2, 1, 8, 2, 128, 8, 100, pkd.BF16), "page_size"),
+    ((2, 4, 32, 8, 128, 16, 100, pkd.FP8_E4M3), "fp8"),
+    ((2, 16, 32, 8, 128, 16, 100, pkd.BF16), "> 32"),
+    ((2, 1, 8, 2, 64, 16, 100, pkd.FP8_E4M3), "head_dim 128"),
+])
+def test_unsupported_plans_are_rejected_with_a_reason(lib, args, needle):
+    with pytest.raises(pkd.PkdError) as e:
+        pkd.workspace_size(*args)
+    assert needle in str(e.value)
+
+
+def test_chunk_must_be_a_page_multiple(lib):
+    with pytest.raises(pkd.PkdError):
+        pkd.workspace_size(2, 1, 8, 2, 128, 16, 100, pkd.BF16, chunk_tokens=24)
+
+
+def _decode_call(lib, **over):
+    a = dict(q=None, q_dt=pkd.BF16, kv=None, kv_dt=pkd.BF16, num_pages=8, bt=None, bt_stride=4, lens=None, B=2,
+             sq=1, Hq=4, Hkv=2, D=64, P=16, max_kv_len=64, scale=0.125, qs=1.0, ks=1.0, vs=1.0, window=0,
+             out=None, out_dt=pkd.BF16, lse=None, ws=None, ws_bytes=1 << 20, chunk=0, flags=0, stream=None)
+    a.update(over)
+    return lib.pkd_paged_decode(*a.values())
+
+
+def test_zero_batch_is_ok_without_a_gpu(lib):
+    assert _decode_call(lib, B=0) == pkd.OK
+
+
+def test_null_pointers_are_einval(lib):
+    assert _decode_call(lib) == pkd.EINVAL
+    assert b"null" in lib.pkd_last_error()
+
+
+def test_mismatched_q_and_cache_types(lib):
+    assert _decode_call(lib, q_dt=pkd.FP16) == pkd.EUNSUPPORTED
+
+
+def test_bad_out_dtype(lib):
+    assert _decode_call(lib, out_dt=pkd.FP8_E4M3) == pkd.EUNSUPPORTED
+
+
+def test_misaligned_and_small_workspace(lib):
+    fake = 1 << 20
+    kw = dict(q=fake, kv=fake, bt=fake, lens=fake, out=fake, ws=fake)
+    assert _decode_call(lib, **dict(kw, kv=fake + 8)) == pkd.EINVAL
+    assert b"misaligned" in lib.pkd_last_error()
+    assert _decode_call(lib, **dict(kw, ws_bytes=256)) == pkd.EINVAL
+    assert b"workspace too small" in lib.pkd_last_error()
+    assert _decode_call(lib, **dict(kw, bt_stride=2)) == pkd.EINVAL
+    assert b"block_table_stride" in lib.pkd_last_error()
+
+
+def test_segmented_validation(lib):
+    seg = lib.pkd_segmented_attention
+    P = None
+    # fp8 is not a segmented dtype
+    assert seg(P, P, P, pkd.FP8_E4M3, P, P, 4, 8, 2, 128, 2, 16, 16, P, P, P, P) == pkd.EUNSUPPORTED
+    # bs not a multiple of 8
+    assert seg(P, P, P, pkd.BF16, P, P, 4, 8, 2, 128, 2, 12, 16, P, P, P, P) == pkd.EUNSUPPORTED
+    # n == 0 is a no-op
+    assert seg(P, P, P, pkd.BF16, P, P, 0, 8, 2, 128, 2, 16, 16, P, P, P, P) == pkd.OK
+    # null inputs
+    assert seg(P, P, P, pkd.BF16, P, P, 4, 8, 2, 128, 2, 16, 16, P, P, P, P) == pkd.EINVAL
+
+
+def test_lse_merge_validation(lib):
+    m = lib.pkd_lse_merge
+    assert m(None, None, None, None, 0, 4, 2, 64, None, pkd.FP32, None, None) == pkd.OK
+    assert m(None, None, None, None, 3, 4, 2, 64, None, pkd.FP32, None, None) == pkd.EINVAL
+    assert m(None, None, None, None, 3, 4, 2, 512, None, pkd.FP32, None, None) == pkd.EUNSUPPORTED

@@ -1,0 +1,215 @@
+"""GPU parity of paged decode against the fp64 oracle, through the C ABI.
+
+Small cases span several 16-key stages, several Split-KV chunks and ragged
+tails; full-size workloads are compared on all (or sampled) requests.  The
+probes check the page gather bit-exactly.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.fail("a CUDA GPU is required for -m gpu tests")
+    import paged_kv_decode_15_gb300 as pkd
+    pkd.build()
+    pkd.load_library()
+
+
+def _check(case, tol=None, batch_index=None, **kw):
+    out, lse = gu.run_paged(case, **kw)
+    ref, rlse = gu.oracle_paged(case, batch_index)
+    if batch_index is not None:
+        out, lse = out[batch_index], lse[batch_index]
+    tol = tol or (gu.TOL_OUT_FP8 if case.dtype == "fp8" else gu.TOL_OUT)
+    e1 = gu.assert_close(out, ref, tol, f"{case.name} out")
+    e2 = gu.assert_close(lse, rlse, gu.TOL_LSE, f"{case.name} lse")
+    return e1, e2
+
+
+LENS = [1, 15, 16, 17, 200, 1000, 777, 64, 0, 333]
+
+SMALL = {
+    # name: paged_case kwargs, call kwargs
+    "bf16_g4_fma": (dict(seq_lens=LENS), dict()),
+    "bf16_g4_mma": (dict(seq_lens=LENS), dict(mma_small_m=True)),
+    "bf16_g4_fma_chunk16": (dict(seq_lens=LENS), dict(chunk_tokens=16)),
+    "bf16_g4_mma_chunk32": (dict(seq_lens=LENS), dict(chunk_tokens=32, mma_small_m=True)),
+    "fp16_g4_fma": (dict(seq_lens=LENS, dtype="fp16"), dict(chunk_tokens=64)),
+    "fp16_g4_mma": (dict(seq_lens=LENS, dtype="fp16"), dict(mma_small_m=True, chunk_tokens=128)),
+    "bf16_d64_p32": (dict(seq_lens=LENS, head_dim=64, page_size=32), dict(chunk_tokens=64)),
+    "bf16_d64_p32_mma": (dict(seq_lens=LENS, head_dim=64, page_size=32), dict(mma_small_m=True)),
+    "bf16_mha_g1": (dict(seq_lens=LENS, num_heads=8, num_kv_heads=8), dict(chunk_tokens=48)),
+    "bf16_g2_sq1": (dict(seq_lens=LENS, num_heads=4, num_kv_heads=2), dict()),
+    "bf16_g8_fma": (dict(seq_lens=LENS, num_heads=64, num_kv_heads=8), dict(chunk_tokens=96)),
+    "bf16_g8_mma": (dict(seq_lens=LENS, num_heads=64, num_kv_heads=8), dict(mma_small_m=True)),
+    "bf16_sq3_g4_m12": (dict(seq_lens=LENS, sq=3), dict(chunk_tokens=64)),
+    "bf16_sq8_g4_m32": (dict(seq_lens=LENS, sq=8), dict(chunk_tokens=128)),
+    "bf16_sq8_g4_m32_auto": (dict(seq_lens=LENS, sq=8), dict()),
+    "bf16_sq5_g4_m20": (dict(seq_lens=LENS, sq=5, head_dim=64), dict(chunk_tokens=64)),
+    "bf16_sq8_window100": (dict(seq_lens=LENS, sq=8, window=100), dict(chunk_tokens=32)),
+    "bf16_sq1_window40_fma": (dict(seq_lens=LENS, window=40), dict()),
+    "bf16_p64_window300": (dict(seq_lens=LENS, page_size=64, window=300), dict(chunk_tokens=128)),
+    "bf16_causal_sq4_m16": (dict(seq_lens=LENS, sq=4, causal=True), dict(chunk_tokens=64)),
+    "bf16_causal_sq4_window50": (dict(seq_lens=LENS, sq=4, causal=True, window=50), dict(chunk_tokens=32)),
+    "bf16_causal_sq2_g2_fma": (dict(seq_lens=LENS, sq=2, num_heads=4, num_kv_heads=2, causal=True, window=30),
+                               dict()),
+    "fp8_g8": (dict(seq_lens=LENS, dtype="fp8", num_heads=64, num_kv_heads=8), dict(chunk_tokens=64)),
+    "fp8_g4_p64": (dict(seq_lens=LENS, dtype="fp8", page_size=64), dict()),
+    "fp8_g2_window": (dict(seq_lens=LENS, dtype="fp8", num_heads=16, num_kv_heads=8, window=100), dict()),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_small_cases_match_oracle(name):
+    ckw, kw = SMALL[name]
+    case = wl.paged_case(name=name, seed=hash(name) % 1000, **ckw)
+    _check(case, **kw)
+
+
+def test_tiny_workload_both_paths():
+    case = wl.tiny_decode()
+    _check(case)
+    _check(case, mma_small_m=True)
+    _check(case, chunk_tokens=16)
+
+
+def test_results_are_deterministic():
+    case = wl.paged_case(name="det", seq_lens=[900, 4000, 33], seed=3)
+    a = gu.run_paged(case, chunk_tokens=256)
+    b = gu.run_paged(case, chunk_tokens=256)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("mma", [False, True])
+def test_argmax_probe_gathers_bit_exactly(mma):
+    """q equal to one visible key and a huge scale: every other weight underflows
+    to 0 and the output must be that key's V row, bit for bit."""
+    case = wl.paged_case(name="probe", seq_lens=[37, 300, 129], num_heads=8, num_kv_heads=2, window=64,
+                         seed=21, table_width=24)
+    rng = np.random.default_rng(0)
+    P, D = case.page_size, case.head_dim
+    targets = {}
+    for b in range(case.batch):
+        L = int(case.seq_lens[b])
+        start = max(0, (L - 64) // P) * P
+        cands = [start, L - 1] + list(rng.integers(start, L, size=2))
+        for h in range(case.num_heads):
+            t = int(cands[h % len(cands)])
+            page = case.block_table[b, t // P]
+            case.q[b, 0, h] = case.kv_cache[page, h // 4, t % P, :D]
+            targets[(b, h)] = (page, h // 4, t % P)
+    case.scale = 100.0
+    out, _ = gu.run_paged(case, mma_small_m=mma, chunk_tokens=32)
+    got_bits = torch.from_numpy(out).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    for (b, h), (page, hk, slot) in targets.items():
+        assert np.array_equal(got_bits[b, 0, h], case.kv_cache[page, hk, slot, D:]), (b, h)
+
+
+@pytest.mark.parametrize("mma", [False, True])
+def test_constant_v_is_exact_and_nan_pages_are_never_read(mma):
+    case = wl.paged_case(name="constv", seq_lens=[37, 300, 1, 129, 700], seed=5)
+    one = 0x3F80
+    P, D = case.page_size, case.head_dim
+    for b in range(case.batch):
+        for j in range(int(case.seq_lens[b])):
+            case.kv_cache[case.block_table[b, j // P], :, j % P, D:] = one
+    out, lse = gu.run_paged(case, mma_small_m=mma, chunk_tokens=64)
+    assert np.all(out == 1.0)
+    assert np.all(np.isfinite(lse))
+
+
+def test_out_dtypes_and_no_lse():
+    import paged_kv_decode_15_gb300 as pkd
+    case = wl.paged_case(name="dt", seq_lens=[100, 513], seed=8)
+    q = gu.to_dev(case.q, "bf16")
+    cache = gu.to_dev(case.kv_cache, "bf16")
+    bt = gu.to_dev(case.block_table, "int32")
+    lens = gu.to_dev(case.seq_lens, "int32")
+    ref, _ = gu.oracle_paged(case)
+    for odt in (torch.float32, torch.float16, torch.bfloat16):
+        out = torch.empty(q.shape, dtype=odt, device="cuda")
+        pkd.paged_decode(q, cache, bt, lens, case.scale, 0, out=out)
+        torch.cuda.synchronize()
+        gu.assert_close(out.double().cpu().numpy(), ref, gu.TOL_OUT, str(odt))
+
+
+def test_bad_lengths_and_pages_raise_the_status_word():
+    import paged_kv_decode_15_gb300 as pkd
+    case = wl.paged_case(name="bad", seq_lens=[100, 50], seed=9, table_width=8)
+    q = gu.to_dev(case.q, "bf16")
+    cache = gu.to_dev(case.kv_cache, "bf16")
+    bt = gu.to_dev(case.block_table, "int32")
+    lens = gu.to_dev(case.seq_lens, "int32")
+    ws = torch.zeros(pkd.workspace_size(2, 1, 32, 8, 128, 16, 128, pkd.BF16), dtype=torch.uint8, device="cuda")
+    out, lse = pkd.paged_decode(q, cache, bt, lens, case.scale, 0, max_kv_len=128, workspace=ws)
+    assert pkd.workspace_check(ws) == pkd.OK
+    lens[0] = 500  # above max_kv_len: clamped and reported
+    pkd.paged_decode(q, cache, bt, lens, case.scale, 0, max_kv_len=128, workspace=ws)
+    assert pkd.workspace_check(ws) == pkd.EDEVICE_BOUNDS
+    assert pkd.workspace_check(ws) == pkd.OK  # the word was cleared
+    lens[0] = 100
+    bt[1, 1] = case.num_pages + 7  # a page outside the pool: its keys are skipped and reported
+    out, lse = pkd.paged_decode(q, cache, bt, lens, case.scale, 0, max_kv_len=128, workspace=ws)
+    assert pkd.workspace_check(ws) == pkd.EDEVICE_BOUNDS
+    assert torch.isfinite(out.float()).all()
+
+
+def test_cuda_graph_replay_follows_new_lengths():
+    """The call records no host state: a captured graph replays correctly when
+    the lengths and the table change in place."""
+    import paged_kv_decode_15_gb300 as pkd
+    case = wl.paged_case(name="graph", seq_lens=[500, 1200, 64, 2048], seed=10, table_width=160)
+    q = gu.to_dev(case.q, "bf16")
+    cache = gu.to_dev(case.kv_cache, "bf16")
+    bt = gu.to_dev(case.block_table, "int32")
+    lens = gu.to_dev(case.seq_lens, "int32")
+    out = torch.empty(q.shape, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device="cuda")
+    ws = torch.empty(pkd.workspace_size(4, 1, 32, 8, 128, 16, 2560, pkd.BF16), dtype=torch.uint8, device="cuda")
+    pkd.workspace_init(ws)
+    kw = dict(out=out, lse=lse, workspace=ws, max_kv_len=2560)
+    pkd.paged_decode(q, cache, bt, lens, case.scale, 0, **kw)  # warm-up outside capture
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            pkd.paged_decode(q, cache, bt, lens, case.scale, 0, **kw)
+    new_lens = np.array([2000, 17, 1024, 2048], np.int32)
+    lens.copy_(torch.from_numpy(new_lens))
+    g.replay()
+    torch.cuda.synchronize()
+    case.seq_lens = new_lens
+    ref, rlse = gu.oracle_paged(case)
+    gu.assert_close(out.double().cpu().numpy(), ref, gu.TOL_OUT, "graph out")
+    gu.assert_close(lse.double().cpu().numpy(), rlse, gu.TOL_LSE, "graph lse")
+
+
+# ------------------------------------------------------ full-size workloads
+def test_gqa_decode_b64_full():
+    case = wl.gqa_decode_b64()
+    _check(case)
+
+
+def test_gqa_decode_b64_tensor_core_variant():
+    case = wl.gqa_decode_b64()
+    _check(case, mma_small_m=True)
+
+
+@pytest.mark.parametrize("window", [0, 4096])
+def test_query_block_sq8_sampled(window):
+    case = wl.query_block_sq8(window=window)
+    _check(case, batch_index=[0, 5, 11, 17, 23, 31])
+
+
+def test_fp8_long_b8_sampled():
+    case = wl.fp8_long_b8()
+    _check(case, batch_index=[0, 7])

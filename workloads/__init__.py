@@ -266,6 +266,24 @@ def dash_segments_n256() -> SegmentCase:
     return segment_case(name="dash_segments_n256", seed=WORKLOAD_SEEDS["dash_segments_n256"])
 
 
+def to_torch(a: np.ndarray, dtype: str, device="cuda") -> torch.Tensor:
+    """Storage array -> torch tensor on `device` (bf16/fp16 as themselves, fp8 as uint8)."""
+    a = np.ascontiguousarray(a)
+    if dtype == "bf16":
+        t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    elif dtype == "fp16":
+        t = torch.from_numpy(a.view(np.int16)).view(torch.float16)
+    elif dtype == "fp8":
+        t = torch.from_numpy(a.view(np.uint8))
+    elif dtype == "int32":
+        t = torch.from_numpy(a.astype(np.int32))
+    elif dtype == "fp32":
+        t = torch.from_numpy(a.astype(np.float32))
+    else:
+        raise ValueError(dtype)
+    return t.to(device)
+
+
 WORKLOADS = {
     "tiny_decode": tiny_decode,
     "gqa_decode_b64": gqa_decode_b64,
