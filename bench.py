@@ -149,7 +149,7 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------ device side
-def _device_inputs(case, torch):
+def _device_inputs(case, torch, chunk=0, path="auto"):
     import paged_kv_decode_15_gb300 as pkd
     from workloads import to_torch
     q = to_torch(case.q, case.dtype)
@@ -160,19 +160,21 @@ def _device_inputs(case, torch):
     lse = torch.empty(case.q.shape[:3], dtype=torch.float32, device="cuda")
     max_kv_len = int(case.block_table.shape[1] * case.page_size)
     kv_code = {"bf16": pkd.BF16, "fp16": pkd.FP16, "fp8": pkd.FP8_E4M3}[case.dtype]
-    flags = pkd.FLAG_CAUSAL if case.causal else 0
+    flags = (pkd.FLAG_CAUSAL if case.causal else 0) | (pkd.FLAG_MMA_SMALL_M if path == "mma" else 0) | \
+        (pkd.FLAG_FMA if path == "fma" else 0)
     ws = torch.empty(pkd.workspace_size(case.batch, case.sq, case.num_heads, case.num_kv_heads, case.head_dim,
-                                        case.page_size, max_kv_len, kv_code, case.window, 0, flags),
+                                        case.page_size, max_kv_len, kv_code, case.window, chunk, flags),
                      dtype=torch.uint8, device="cuda")
     pkd.workspace_init(ws)
-    return dict(q=q, cache=cache, bt=bt, lens=lens, out=out, lse=lse, ws=ws, max_kv_len=max_kv_len)
+    return dict(q=q, cache=cache, bt=bt, lens=lens, out=out, lse=lse, ws=ws, max_kv_len=max_kv_len, chunk=chunk,
+                path=path)
 
 
-def _call(case, d, pkd, q=None, bt=None, lens=None):
-    pkd.paged_decode(q if q is not None else d["q"], d["cache"], bt if bt is not None else d["bt"],
-                     lens if lens is not None else d["lens"], case.scale, case.window, out=d["out"],
+def _call(case, d, pkd):
+    pkd.paged_decode(d["q"], d["cache"], d["bt"], d["lens"], case.scale, case.window, out=d["out"],
                      lse=d["lse"], q_scale=case.q_scale, k_scale=case.k_scale, v_scale=case.v_scale,
-                     max_kv_len=d["max_kv_len"], workspace=d["ws"], causal=case.causal)
+                     max_kv_len=d["max_kv_len"], workspace=d["ws"], causal=case.causal,
+                     chunk_tokens=d["chunk"], mma_small_m=d["path"] == "mma", force_fma=d["path"] == "fma")
 
 
 def run_gpu(args, rank, world, dist):
@@ -184,7 +186,7 @@ def run_gpu(args, rank, world, dist):
     pkd.load_library()
     case = wl.WORKLOADS[args.workload]()
     acct = algorithmic_bytes(case)
-    d = _device_inputs(case, torch)
+    d = _device_inputs(case, torch, args.chunk, args.path)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
 
@@ -244,11 +246,21 @@ def run_gpu(args, rank, world, dist):
         raise RuntimeError("device status word set: " + pkd.load_library().pkd_last_error().decode())
 
     if dist:
-        import torch.distributed as tdist
-        t = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device="cuda")
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        total_ms, e2e_ms = float(t[0]), float(t[1])
+        total_ms, e2e_ms = max_over_ranks([total_ms, e2e_ms], dist, "cuda")
     return case, acct, step_ms, total_ms, e2e_ms, h2d, d2h, clocks
+
+
+def max_over_ranks(values, dist, device):
+    """Element-wise max of per-rank timings (the slowest replica sets the job time)."""
+    import torch
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def job_throughput(bytes_per_step_per_rank: int, world: int, steps: int, total_ms: float) -> float:
+    """Whole-job GB/s: every rank's bytes over the slowest rank's time."""
+    return bytes_per_step_per_rank * world * steps / (total_ms / 1e3) / 1e9
 
 
 def cpu_baseline(case, budget_s: float = 12.0) -> dict:
@@ -324,7 +336,8 @@ def workload_config(case, args) -> dict:
                          "total": int(case.seq_lens.sum())},
             "pool_pages": case.num_pages, "l2": "L2 flushed (512 MiB write) before every timed step; "
                                                 "KV stream larger than L2",
-            "parallelism": f"replicas{args.gpus}" if args.gpus > 1 else "single"}
+            "parallelism": f"replicas{args.gpus}" if args.gpus > 1 else "single",
+            "kernel_path": getattr(args, "path", "auto"), "chunk_tokens": getattr(args, "chunk", 0)}
 
 
 def main():
@@ -335,6 +348,9 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="pkd", choices=["pkd", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--chunk", type=int, default=0, help="Split-KV chunk in keys (0 = the library's plan)")
+    ap.add_argument("--path", default="auto", choices=["auto", "mma", "fma"],
+                    help="kernel for small M: library default, tensor cores, or CUDA cores")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -355,7 +371,7 @@ def main():
     if rank == 0:
         peaks = load_peaks()
         steps = args.steps
-        gbs = acct["kv"] * world * steps / (total_ms / 1e3) / 1e9
+        gbs = job_throughput(acct["kv"], world, steps, total_ms)
         avg_ms = total_ms / steps
         achieved = acct["total"] / (avg_ms / 1e3) / 1e9
         traffic = profiled_traffic(case.name)
@@ -369,7 +385,7 @@ def main():
                          "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
                          "algorithmic_bytes_per_launch": acct["total"], "peak_source": peaks["source"],
                          "kernel": "paged decode (one launch per step)"},
-            "e2e": {"value": round(acct["kv"] * world * steps / (e2e_ms / 1e3) / 1e9, 2), "unit": "GB/s",
+            "e2e": {"value": round(job_throughput(acct["kv"], world, steps, e2e_ms), 2), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "us_per_call": round(e2e_ms / steps * 1e3, 2),
                     "note": "q, block_table, seq_lens in from pinned host memory, out and lse back, every step; "

@@ -389,6 +389,7 @@ pkd_status pkd_lse_merge(const float* part_out, const float* part_lse, const flo
     p.live = live;
     p.n = n;
     p.parts = parts;
+    p.prior_cols = parts;
     p.heads = heads;
     p.D = head_dim;
     p.out = out;

@@ -166,7 +166,9 @@ def test_cuda_graph_replay_follows_new_lengths():
     """The call records no host state: a captured graph replays correctly when
     the lengths and the table change in place."""
     import paged_kv_decode_15_gb300 as pkd
-    case = wl.paged_case(name="graph", seq_lens=[500, 1200, 64, 2048], seed=10, table_width=160)
+    # pages are allocated for the longest lengths either pass uses
+    case = wl.paged_case(name="graph", seq_lens=[2000, 1200, 1024, 2048], seed=10, table_width=160)
+    case.seq_lens = np.array([500, 1200, 64, 2048], np.int32)
     q = gu.to_dev(case.q, "bf16")
     cache = gu.to_dev(case.kv_cache, "bf16")
     bt = gu.to_dev(case.block_table, "int32")
