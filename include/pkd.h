@@ -133,6 +133,36 @@ pkd_status pkd_paged_decode(const void* q, pkd_dtype q_dtype,
                             unsigned flags, void* stream);
 
 /*
+ * pkd_paged_decode without a caller workspace.  The pages have no counterpart
+ * of this call: it exists for callers that cannot allocate device memory at
+ * the point where they run decode -- code running while a CUDA graph is being
+ * captured (allocation is not a capturable operation), plug-ins whose host
+ * runtime owns all device memory, or C callers with no device allocator of
+ * their own.
+ *
+ * It takes the same arguments as pkd_paged_decode minus the workspace and
+ * uses instead a scratch array compiled into the library: 32 MiB of device
+ * memory that every GPU loading the library holds until the process exits.
+ * A plan whose workspace (pkd_paged_decode_workspace_size) exceeds 32 MiB is
+ * rejected with PKD_EUNSUPPORTED.  The call allocates nothing; it clears the
+ * part of the scratch it uses (cudaMemsetAsync on `stream`) and launches the
+ * decode kernel.  The first call on each device looks up the scratch
+ * address on that device (make it before any stream capture).  All calls
+ * share the one scratch array: calls that may overlap on the GPU (different
+ * streams, or different host threads on one device) race and must be
+ * serialised by the caller.  The device-side status word is not reported.
+ */
+pkd_status pkd_paged_decode_static(const void* q, pkd_dtype q_dtype,
+                                   const void* kv_cache, pkd_dtype kv_dtype, int64_t num_pages,
+                                   const int32_t* block_table, int64_t block_table_stride,
+                                   const int32_t* seq_lens,
+                                   int batch, int sq, int num_heads, int num_kv_heads, int head_dim,
+                                   int page_size, int max_kv_len,
+                                   float scale, float q_scale, float k_scale, float v_scale, int window,
+                                   void* out, pkd_dtype out_dtype, float* lse,
+                                   int chunk_tokens, unsigned flags, void* stream);
+
+/*
  * DASH segmented attention with its combine [DASH flash_dash_attention].
  *
  *   q        device [n, num_heads, head_dim], dtype (bf16 or fp16)

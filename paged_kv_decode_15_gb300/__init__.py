@@ -25,7 +25,8 @@ BF16, FP16, FP8_E4M3, FP32 = 0, 1, 2, 3
 FLAG_CAUSAL, FLAG_MMA_SMALL_M, FLAG_FMA = 1, 2, 4
 
 SYMBOLS = ("pkd_version", "pkd_last_error", "pkd_paged_decode_workspace_size", "pkd_workspace_init",
-           "pkd_workspace_check", "pkd_paged_decode", "pkd_segmented_attention", "pkd_lse_merge")
+           "pkd_workspace_check", "pkd_paged_decode", "pkd_paged_decode_static", "pkd_segmented_attention",
+           "pkd_lse_merge")
 
 
 class PkdError(RuntimeError):
@@ -62,10 +63,12 @@ def load_library(path: str = LIB_PATH):
     lib.pkd_workspace_check.argtypes = [P, SZ, P]
     lib.pkd_paged_decode.argtypes = [P, I, P, I, I64, P, I64, P, I, I, I, I, I, I, I, F, F, F, F, I,
                                      P, I, P, P, SZ, I, U, P]
+    lib.pkd_paged_decode_static.argtypes = [P, I, P, I, I64, P, I64, P, I, I, I, I, I, I, I, F, F, F, F, I,
+                                            P, I, P, I, U, P]
     lib.pkd_segmented_attention.argtypes = [P, P, P, I, P, P, I, I, I, I, I, I, I, P, P, P, P]
     lib.pkd_lse_merge.argtypes = [P, P, P, P, I, I, I, I, P, I, P, P]
-    for name in ("pkd_workspace_init", "pkd_workspace_check", "pkd_paged_decode", "pkd_segmented_attention",
-                 "pkd_lse_merge"):
+    for name in ("pkd_workspace_init", "pkd_workspace_check", "pkd_paged_decode", "pkd_paged_decode_static",
+                 "pkd_segmented_attention", "pkd_lse_merge"):
         getattr(lib, name).restype = I
     _lib = lib
     return lib

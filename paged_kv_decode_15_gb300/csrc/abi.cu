@@ -198,6 +198,16 @@ pkd_status get_map(CUtensorMap& out, const void* base, int rank, uint64_t d0, ui
 
 }  // namespace
 
+int pkd::report_status(int st, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
 extern "C" {
 
 int pkd_version(void) { return 10000; }

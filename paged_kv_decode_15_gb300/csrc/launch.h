@@ -4,6 +4,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "../../include/pkd.h"
+
 namespace pkd {
 
 struct DecodeParams;
@@ -18,6 +20,13 @@ cudaError_t launch_decode_mma(int D, bool bf16, int MT, int NT, const CUtensorMa
                               const DecodeParams& p, dim3 grid, cudaStream_t stream);
 cudaError_t launch_decode_fma(int D, int kvt, int LPT, int MR, const CUtensorMap& tmap,
                               const DecodeParams& p, dim3 grid, cudaStream_t stream);
+
+// Record `fmt` as this thread's last error message and return `st`.
+int report_status(int st, const char* fmt, ...);
+template <class... A>
+inline pkd_status report(pkd_status st, const char* fmt, A... a) {
+    return static_cast<pkd_status>(report_status(static_cast<int>(st), fmt, a...));
+}
 
 struct SegmentParams;
 struct MergeParams;
