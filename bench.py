@@ -149,32 +149,133 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------ device side
-def _device_inputs(case, torch, chunk=0, path="auto"):
-    import paged_kv_decode_15_gb300 as pkd
-    from workloads import to_torch
-    q = to_torch(case.q, case.dtype)
-    cache = to_torch(case.kv_cache, case.dtype)
-    bt = to_torch(case.block_table, "int32")
-    lens = to_torch(case.seq_lens, "int32")
-    out = torch.empty(case.q.shape, dtype=torch.bfloat16 if case.dtype != "fp16" else torch.float16, device="cuda")
-    lse = torch.empty(case.q.shape[:3], dtype=torch.float32, device="cuda")
-    max_kv_len = int(case.block_table.shape[1] * case.page_size)
-    kv_code = {"bf16": pkd.BF16, "fp16": pkd.FP16, "fp8": pkd.FP8_E4M3}[case.dtype]
-    flags = (pkd.FLAG_CAUSAL if case.causal else 0) | (pkd.FLAG_MMA_SMALL_M if path == "mma" else 0) | \
-        (pkd.FLAG_FMA if path == "fma" else 0)
-    ws = torch.empty(pkd.workspace_size(case.batch, case.sq, case.num_heads, case.num_kv_heads, case.head_dim,
-                                        case.page_size, max_kv_len, kv_code, case.window, chunk, flags),
-                     dtype=torch.uint8, device="cuda")
-    pkd.workspace_init(ws)
-    return dict(q=q, cache=cache, bt=bt, lens=lens, out=out, lse=lse, ws=ws, max_kv_len=max_kv_len, chunk=chunk,
-                path=path)
+class PagedRunner:
+    """One paged_decode call over a PagedCase, inputs resident on the device."""
+    kernel = "paged decode (one launch per step)"
+
+    def __init__(self, case, args, torch, pkd):
+        from workloads import to_torch
+        self.case, self.pkd = case, pkd
+        self.q = to_torch(case.q, case.dtype)
+        self.cache = to_torch(case.kv_cache, case.dtype)
+        self.bt = to_torch(case.block_table, "int32")
+        self.lens = to_torch(case.seq_lens, "int32")
+        self.out = torch.empty(case.q.shape, dtype=torch.bfloat16 if case.dtype != "fp16" else torch.float16,
+                               device="cuda")
+        self.lse = torch.empty(case.q.shape[:3], dtype=torch.float32, device="cuda")
+        self.max_kv_len = int(case.block_table.shape[1] * case.page_size)
+        kv_code = {"bf16": pkd.BF16, "fp16": pkd.FP16, "fp8": pkd.FP8_E4M3}[case.dtype]
+        self.chunk, self.path, self.grid = args.chunk, args.path, args.grid
+        flags = (pkd.FLAG_CAUSAL if case.causal else 0) | (pkd.FLAG_FMA if self.path == "fma" else 0) | \
+            (pkd.FLAG_GRID if self.grid else 0)
+        self.ws = torch.empty(pkd.workspace_size(case.batch, case.sq, case.num_heads, case.num_kv_heads,
+                                                 case.head_dim, case.page_size, self.max_kv_len, kv_code, case.window,
+                                                 self.chunk, flags), dtype=torch.uint8, device="cuda")
+        pkd.workspace_init(self.ws)
+        self.inputs = [self.q, self.bt, self.lens]   # copied in every end-to-end step
+        self.outputs = [self.out, self.lse]          # copied back every end-to-end step
+        self.acct = algorithmic_bytes(case)
+
+    def call(self):
+        c = self.case
+        self.pkd.paged_decode(self.q, self.cache, self.bt, self.lens, c.scale, c.window, out=self.out, lse=self.lse,
+                              q_scale=c.q_scale, k_scale=c.k_scale, v_scale=c.v_scale, max_kv_len=self.max_kv_len,
+                              workspace=self.ws, causal=c.causal, chunk_tokens=self.chunk,
+                              force_fma=self.path == "fma", grid=self.grid)
+
+    def check(self):
+        if self.pkd.workspace_check(self.ws) != self.pkd.OK:
+            raise RuntimeError("device status word set: " + self.pkd.load_library().pkd_last_error().decode())
 
 
-def _call(case, d, pkd):
-    pkd.paged_decode(d["q"], d["cache"], d["bt"], d["lens"], case.scale, case.window, out=d["out"],
-                     lse=d["lse"], q_scale=case.q_scale, k_scale=case.k_scale, v_scale=case.v_scale,
-                     max_kv_len=d["max_kv_len"], workspace=d["ws"], causal=case.causal,
-                     chunk_tokens=d["chunk"], mma_small_m=d["path"] == "mma", force_fma=d["path"] == "fma")
+class SegmentRunner:
+    """One segmented_attention call (attention per segment + combine)."""
+    kernel = "DASH segmented attention with fused combine (one launch per step)"
+
+    def __init__(self, case, args, torch, pkd):
+        from workloads import to_torch
+        self.case, self.pkd = case, pkd
+        self.q = to_torch(case.q, case.dtype)
+        self.k = to_torch(case.k, case.dtype)
+        self.v = to_torch(case.v, case.dtype)
+        self.used = to_torch(case.used, "int32")
+        self.bias = to_torch(case.bias, "fp32")
+        self.out = torch.empty_like(self.q)
+        self.inputs = [self.q, self.k, self.v, self.used, self.bias]
+        self.outputs = [self.out]
+        self.acct = segment_bytes(case)
+
+    def call(self):
+        self.pkd.segmented_attention(self.q, self.k, self.v, self.used, self.bias, self.case.bs, self.case.local,
+                                     out=self.out)
+
+    def check(self):
+        pass
+
+
+class PagedSegmentRunner:
+    """One segmented_attention_paged call: segments read through the block table."""
+    kernel = "DASH segmented attention from the paged cache, fused combine (one launch per step)"
+
+    def __init__(self, case, args, torch, pkd):
+        from workloads import to_torch
+        self.case, self.pkd = case, pkd
+        self.q = to_torch(case.q, case.dtype)
+        self.cache = to_torch(case.kv_cache, case.dtype)
+        self.bt = to_torch(case.block_table, "int32")
+        self.seg_start = to_torch(case.seg_start, "int32")
+        self.used = to_torch(case.used, "int32")
+        self.bias = to_torch(case.bias, "fp32")
+        self.out = torch.empty_like(self.q)
+        self.inputs = [self.q, self.bt, self.seg_start, self.used, self.bias]
+        self.outputs = [self.out]
+        Hkv, D = case.num_kv_heads, case.q.shape[2]
+        kv = int(case.used.sum()) * Hkv * 2 * D * 2
+        self.acct = {"kv": kv, "total": kv + case.q.nbytes * 2 + case.used.nbytes * 2 + case.bias.nbytes}
+
+    def call(self):
+        c = self.case
+        self.pkd.segmented_attention_paged(self.q, self.cache, self.bt, self.seg_start, self.used, self.bias, c.bs,
+                                           c.local, out=self.out)
+
+    def check(self):
+        pass
+
+
+class CacheWriteRunner:
+    """One cache_write call: new key/value rows quantised into their slots."""
+    kernel = "KV-cache write (one launch per step)"
+
+    def __init__(self, case, args, torch, pkd):
+        from workloads import to_torch
+        self.case, self.pkd = case, pkd
+        self.key = to_torch(case.key, case.in_dtype)
+        self.value = to_torch(case.value, case.in_dtype)
+        self.slots = torch.from_numpy(case.slots).cuda()
+        self.cache = to_torch(case.kv_cache, case.kv_dtype)
+        self.inputs = [self.key, self.value, self.slots]
+        self.outputs = []
+        live = int((case.slots >= 0).sum())
+        Hkv, D = case.key.shape[1], case.key.shape[2]
+        out_elt = 1 if case.kv_dtype == "fp8" else 2
+        kv = live * Hkv * 2 * D * (2 + out_elt)
+        self.acct = {"kv": kv, "total": kv + case.slots.nbytes}
+
+    def call(self):
+        self.pkd.cache_write(self.key, self.value, self.slots, self.cache, k_scale=self.case.k_scale,
+                             v_scale=self.case.v_scale)
+
+    def check(self):
+        pass
+
+
+def segment_bytes(case) -> dict:
+    """Algorithmic bytes of segmented attention: the used K and V rows of every
+    segment for every kv head, plus q, out, used and bias."""
+    elt = 2
+    kv = int(np.clip(case.used, 0, None).sum()) * case.num_kv_heads * 2 * case.q.shape[2] * elt
+    extra = case.q.nbytes * 2 + case.used.nbytes + case.bias.nbytes
+    return {"kv": kv, "total": kv + extra}
 
 
 def run_gpu(args, rank, world, dist):
@@ -185,17 +286,18 @@ def run_gpu(args, rank, world, dist):
     pkd.build()
     pkd.load_library()
     case = wl.WORKLOADS[args.workload]()
-    acct = algorithmic_bytes(case)
-    d = _device_inputs(case, torch, args.chunk, args.path)
+    kind = SegmentRunner if isinstance(case, wl.SegmentCase) else \
+        CacheWriteRunner if isinstance(case, wl.CacheWriteCase) else \
+        PagedSegmentRunner if isinstance(case, wl.PagedSegmentCase) else PagedRunner
+    runner = kind(case, args, torch, pkd)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
 
     for _ in range(args.warmup):
         flush.zero_()
-        _call(case, d, pkd)
+        runner.call()
     torch.cuda.synchronize()
-    if pkd.workspace_check(d["ws"]) != pkd.OK:
-        raise RuntimeError("device status word set during warm-up: " + pkd.load_library().pkd_last_error().decode())
+    runner.check()
 
     sampler = ClockSampler(torch.cuda.current_device())
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -207,7 +309,7 @@ def run_gpu(args, rank, world, dist):
     for i in range(args.steps):
         flush.zero_()
         starts[i].record(stream)
-        _call(case, d, pkd)
+        runner.call()
         ends[i].record(stream)
     torch.cuda.synchronize()
     t1 = time.time()
@@ -218,36 +320,29 @@ def run_gpu(args, rank, world, dist):
     total_ms = float(sum(step_ms))
 
     # end to end through the public call: pinned host inputs in, results out
-    qh = torch.empty(d["q"].shape, dtype=d["q"].dtype, pin_memory=True).copy_(d["q"].cpu())
-    bth = torch.empty(d["bt"].shape, dtype=torch.int32, pin_memory=True).copy_(d["bt"].cpu())
-    lensh = torch.empty(d["lens"].shape, dtype=torch.int32, pin_memory=True).copy_(d["lens"].cpu())
-    outh = torch.empty(d["out"].shape, dtype=d["out"].dtype, pin_memory=True)
-    lseh = torch.empty(d["lse"].shape, dtype=torch.float32, pin_memory=True)
-    h2d = qh.nbytes + bth.nbytes + lensh.nbytes
-    d2h = outh.nbytes + lseh.nbytes
-    e2e_steps = args.steps
-    es = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
-    ee = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    host_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu()) for t in runner.inputs]
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in runner.outputs]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    es = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ee = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     torch.cuda.synchronize()
-    for i in range(e2e_steps):
+    for i in range(args.steps):
         flush.zero_()
         es[i].record(stream)
-        d["q"].copy_(qh, non_blocking=True)
-        d["bt"].copy_(bth, non_blocking=True)
-        d["lens"].copy_(lensh, non_blocking=True)
-        _call(case, d, pkd)
-        outh.copy_(d["out"], non_blocking=True)
-        lseh.copy_(d["lse"], non_blocking=True)
+        for dev, host in zip(runner.inputs, host_in):
+            dev.copy_(host, non_blocking=True)
+        runner.call()
+        for dev, host in zip(runner.outputs, host_out):
+            host.copy_(dev, non_blocking=True)
         ee[i].record(stream)
     torch.cuda.synchronize()
     e2e_ms = float(sum(s.elapsed_time(e) for s, e in zip(es, ee)))
-    status = pkd.workspace_check(d["ws"])
-    if status != pkd.OK:
-        raise RuntimeError("device status word set: " + pkd.load_library().pkd_last_error().decode())
+    runner.check()
 
     if dist:
         total_ms, e2e_ms = max_over_ranks([total_ms, e2e_ms], dist, "cuda")
-    return case, acct, step_ms, total_ms, e2e_ms, h2d, d2h, clocks
+    return case, runner, step_ms, total_ms, e2e_ms, h2d, d2h, clocks
 
 
 def max_over_ranks(values, dist, device):
@@ -329,6 +424,20 @@ def run_reference(args, rank):
 
 
 def workload_config(case, args) -> dict:
+    if hasattr(case, "slots"):
+        return {"workload": case.name, "num_tokens": case.num_tokens, "num_kv_heads": case.key.shape[1],
+                "head_dim": case.key.shape[2], "page_size": case.page_size, "in_dtype": case.in_dtype,
+                "kv_dtype": case.kv_dtype, "l2": "L2 flushed (512 MiB write) before every timed step"}
+    if hasattr(case, "seg_start"):
+        return {"workload": case.name, "n": case.n, "num_heads": case.q.shape[1], "num_kv_heads": case.num_kv_heads,
+                "head_dim": case.q.shape[2], "page_size": case.page_size, "topk": case.topk, "bs": case.bs,
+                "local": case.local, "dtype": case.dtype, "used_keys": int(case.used.sum()),
+                "l2": "L2 flushed (512 MiB write) before every timed step"}
+    if not hasattr(case, "seq_lens"):
+        return {"workload": case.name, "n": case.n, "num_heads": case.q.shape[1], "num_kv_heads": case.num_kv_heads,
+                "head_dim": case.q.shape[2], "topk": case.topk, "bs": case.bs, "local": case.local,
+                "dtype": case.dtype, "used_rows": int(case.used.sum()),
+                "l2": "L2 flushed (512 MiB write) before every timed step"}
     return {"workload": case.name, "batch": case.batch, "sq": case.sq, "num_heads": case.num_heads,
             "num_kv_heads": case.num_kv_heads, "head_dim": case.head_dim, "page_size": case.page_size,
             "kv_dtype": case.dtype, "window": case.window, "causal": case.causal,
@@ -337,7 +446,8 @@ def workload_config(case, args) -> dict:
             "pool_pages": case.num_pages, "l2": "L2 flushed (512 MiB write) before every timed step; "
                                                 "KV stream larger than L2",
             "parallelism": f"replicas{args.gpus}" if args.gpus > 1 else "single",
-            "kernel_path": getattr(args, "path", "auto"), "chunk_tokens": getattr(args, "chunk", 0)}
+            "kernel_path": getattr(args, "path", "auto"), "chunk_tokens": getattr(args, "chunk", 0),
+            "partition": "chunked grid" if getattr(args, "grid", False) else "persistent flat"}
 
 
 def main():
@@ -349,8 +459,10 @@ def main():
     ap.add_argument("--impl", default="pkd", choices=["pkd", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--chunk", type=int, default=0, help="Split-KV chunk in keys (0 = the library's plan)")
-    ap.add_argument("--path", default="auto", choices=["auto", "mma", "fma"],
-                    help="kernel for small M: library default, tensor cores, or CUDA cores")
+    ap.add_argument("--path", default="auto", choices=["auto", "fma"],
+                    help="library default (tensor cores for 16-bit caches) or CUDA cores")
+    ap.add_argument("--grid", action="store_true",
+                    help="one CTA per Split-KV chunk instead of the persistent flat partition")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -367,7 +479,8 @@ def main():
         import torch.distributed as tdist
         tdist.init_process_group(backend="nccl")
         dist = tdist
-    case, acct, step_ms, total_ms, e2e_ms, h2d, d2h, clocks = run_gpu(args, rank, world, dist)
+    case, runner, step_ms, total_ms, e2e_ms, h2d, d2h, clocks = run_gpu(args, rank, world, dist)
+    acct = runner.acct
     if rank == 0:
         peaks = load_peaks()
         steps = args.steps
@@ -378,22 +491,28 @@ def main():
         line = {
             "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world, "steps": steps,
             "warmup": args.warmup, "ms_per_step": round(avg_ms, 5), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": case.dtype, "data": "synthetic", "config": workload_config(case, args),
+            "vs_baseline": None, "dtype": getattr(case, "dtype", getattr(case, "kv_dtype", None)),
+            "data": "synthetic", "config": workload_config(case, args),
             "us_per_call": round(avg_ms * 1e3, 2), "us_per_call_median": round(statistics.median(step_ms) * 1e3, 2),
             "pct_of_hbm_peak": round(100 * gbs / world / peaks["hbm_gbs"], 2),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
                          "algorithmic_bytes_per_launch": acct["total"], "peak_source": peaks["source"],
-                         "kernel": "paged decode (one launch per step)"},
+                         "kernel": runner.kernel},
             "e2e": {"value": round(job_throughput(acct["kv"], world, steps, e2e_ms), 2), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "us_per_call": round(e2e_ms / steps * 1e3, 2),
-                    "note": "q, block_table, seq_lens in from pinned host memory, out and lse back, every step; "
-                            "the KV cache is resident device state"},
+                    "note": ("q, block_table, seq_lens in from pinned host memory, out and lse back, every step; "
+                             "the KV cache is resident device state") if isinstance(runner, PagedRunner) else
+                            ("key, value, slot_mapping in from pinned host memory; the cache is resident "
+                             "device state") if isinstance(runner, CacheWriteRunner) else
+                            ("q, block_table, seg_start, used, bias in, out back; the cache is resident device "
+                             "state") if isinstance(runner, PagedSegmentRunner) else
+                            "q, k, v, used, bias in from pinned host memory and out back, every step"},
             "gpu_launches": steps,
             "clocks": clocks,
         }
-        if not args.no_cpu_baseline:
+        if not args.no_cpu_baseline and isinstance(runner, PagedRunner):
             line["cpu_baseline"] = cpu_baseline(case)
         print(json.dumps(line), flush=True)
     if dist:

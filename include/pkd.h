@@ -45,8 +45,9 @@ typedef enum {
 
 /* Flags for pkd_paged_decode. */
 #define PKD_FLAG_CAUSAL 1u      /* causal mask inside the query block, exact per-token window */
-#define PKD_FLAG_MMA_SMALL_M 2u /* use the tensor-core kernel even when sq*Hq/Hkv < 16 */
-#define PKD_FLAG_FMA 4u         /* force the CUDA-core kernel (only when sq*Hq/Hkv <= 8) */
+#define PKD_FLAG_MMA_SMALL_M 2u /* tensor cores for sq*Hq/Hkv < 16 (the default for 16-bit caches) */
+#define PKD_FLAG_FMA 4u         /* CUDA cores instead (only when sq*Hq/Hkv <= 8; always for fp8) */
+#define PKD_FLAG_GRID 8u        /* one CTA per Split-KV chunk instead of the persistent flat partition */
 
 /* Library version, major*10000 + minor*100 + patch. */
 int pkd_version(void);
@@ -114,12 +115,16 @@ pkd_status pkd_workspace_check(void* workspace, size_t workspace_bytes, void* st
  * ([TS _get_plan] mask_type "causal", window_left = window - 1).
  * A query row with no visible key gets out = 0 and lse = -inf.
  *
- * Long sequences are split into chunks of chunk_tokens keys whose partial
- * results are merged by LSE inside the same launch [FA num_splits].
+ * Split-KV [FA num_splits]: the keys of a (request, kv head) may be shared
+ * between several workers whose partial results are merged by LSE inside
+ * the same launch.  For batch <= 1024 a persistent grid gives every warp an
+ * equal slice of all requests' keys laid end to end; otherwise (or with
+ * PKD_FLAG_GRID) one CTA takes each chunk of chunk_tokens keys.
  *
  * Limits: head_dim 64 or 128; page_size a multiple of 16; num_heads a
- * multiple of num_kv_heads; sq * num_heads / num_kv_heads <= 64 (<= 8 for fp8);
- * fp8 caches need head_dim 128.  Anything else: PKD_EUNSUPPORTED.
+ * multiple of num_kv_heads; sq * num_heads / num_kv_heads <= 32 (<= 8 for fp8);
+ * fp8 caches need head_dim 128.  Anything else: PKD_EUNSUPPORTED.  After a
+ * PKD_ETIMEOUT, zero the workspace again before reusing it.
  */
 pkd_status pkd_paged_decode(const void* q, pkd_dtype q_dtype,
                             const void* kv_cache, pkd_dtype kv_dtype, int64_t num_pages,
@@ -163,6 +168,28 @@ pkd_status pkd_paged_decode_static(const void* q, pkd_dtype q_dtype,
                                    int chunk_tokens, unsigned flags, void* stream);
 
 /*
+ * KV-cache write [TS FlashInferTSImpl.do_kv_cache_update, reshape_and_cache_flash]:
+ * the key and value rows of num_tokens new tokens go to their slots.
+ *
+ *   key, value    device [num_tokens, num_kv_heads, head_dim], in_dtype (bf16 or
+ *                 fp16); rows of one token contiguous, key_stride / value_stride
+ *                 elements between tokens (multiples of 8); 16-byte aligned
+ *   slot_mapping  device int64 [num_tokens]: slot s is page s / page_size,
+ *                 offset s % page_size; s < 0 (padding) and slots past the
+ *                 cache write nothing
+ *   kv_cache      device [num_pages, num_kv_heads, page_size, 2*head_dim]
+ *                 kv_dtype: key into [..., :head_dim], value into [..., head_dim:]
+ *
+ * kv_dtype == in_dtype stores the input bits.  PKD_FP8_E4M3 stores
+ * e4m3(x / k_scale) for keys and e4m3(x / v_scale) for values: the quotient is
+ * an IEEE fp32 division, rounded to nearest even and saturated to +-448.
+ */
+pkd_status pkd_cache_write(const void* key, const void* value, pkd_dtype in_dtype, int64_t key_stride,
+                           int64_t value_stride, const int64_t* slot_mapping, int64_t num_tokens,
+                           int num_kv_heads, int head_dim, int page_size, int64_t num_pages,
+                           void* kv_cache, pkd_dtype kv_dtype, float k_scale, float v_scale, void* stream);
+
+/*
  * DASH segmented attention with its combine [DASH flash_dash_attention].
  *
  *   q        device [n, num_heads, head_dim], dtype (bf16 or fp16)
@@ -189,6 +216,34 @@ pkd_status pkd_segmented_attention(const void* q, const void* k, const void* v, 
                                    int n, int num_heads, int num_kv_heads, int head_dim,
                                    int topk, int bs, int local,
                                    void* out, float* seg_out, float* seg_lse, void* stream);
+
+/*
+ * DASH segmented attention read straight from the paged cache: the segments
+ * are key ranges of the query's own request, gathered through the block
+ * table instead of being copied into contiguous k/v first (the copy that
+ * feeds [DASH flash_dash_attention]).
+ *
+ *   q            device [n, num_heads, head_dim], dtype (bf16 or fp16)
+ *   kv_cache     device [num_pages, num_kv_heads, page_size, 2*head_dim], dtype
+ *   block_table  device int32 [n, block_table_stride]: row i is query i's request
+ *   seg_start    device int32 [n, topk+1]: position of the first key of each
+ *                segment in that request ([topk gathered, local] order)
+ *   used         device int32 [n, topk+1]: keys in each segment, clamped to
+ *                [0, bs] (gathered) or [0, local] (local segment) and to max_kv_len
+ *   bias, out, seg_out, seg_lse as for pkd_segmented_attention
+ *
+ * Segment g of query i holds keys [seg_start, seg_start + used) of request i;
+ * everything else (scale, per-segment (o, lse), the combine) is as in
+ * pkd_segmented_attention.  page_size must be a multiple of 16; pages outside
+ * [0, num_pages) are skipped.
+ */
+pkd_status pkd_segmented_attention_paged(const void* q, pkd_dtype dtype, const void* kv_cache,
+                                         int64_t num_pages, const int32_t* block_table,
+                                         int64_t block_table_stride, const int32_t* seg_start,
+                                         const int32_t* used, const float* bias, int n, int num_heads,
+                                         int num_kv_heads, int head_dim, int page_size, int topk, int bs,
+                                         int local, int max_kv_len, void* out, float* seg_out,
+                                         float* seg_lse, void* stream);
 
 /*
  * LSE merge of partial attention results: the Split-KV merge [FA] and, with a

@@ -70,8 +70,12 @@ def _bind(lib):
                                      D, D, D, D, I, I, P, P, I]
     lib.orc_segmented_attention.argtypes = [P, P, P, I, P, P, I, I, I, I, I, I, I, P, P, P, I]
     lib.orc_lse_merge.argtypes = [P, P, P, P, I, I, I, I, P, P]
+    lib.orc_segmented_paged.argtypes = [P, I, P, L, P, L, P, P, P, I, I, I, I, I, I, I, I, P, P, P, I]
+    lib.orc_encode_e4m3.argtypes = [ctypes.c_float]
+    lib.orc_encode_e4m3.restype = ctypes.c_uint8
+    lib.orc_cache_write.argtypes = [P, P, I, P, L, I, I, I, L, P, I, ctypes.c_float, ctypes.c_float]
     for f in ("orc_decode", "orc_restrict_to_window", "orc_paged_decode",
-              "orc_segmented_attention", "orc_lse_merge"):
+              "orc_segmented_attention", "orc_lse_merge", "orc_cache_write", "orc_segmented_paged"):
         getattr(lib, f).restype = I
     return lib
 
@@ -199,3 +203,53 @@ def lse_merge(part_out, part_lse, prior=None, live=None):
     if rc != 0:
         raise ValueError("lse_merge oracle rejected its input")
     return out, lse
+
+
+def encode_e4m3(x) -> np.ndarray:
+    """fp32 values -> e4m3fn codes: round to nearest even, saturating to +-448."""
+    a = np.ascontiguousarray(x, dtype=np.float32).reshape(-1)
+    lib = _load()
+    return np.array([lib.orc_encode_e4m3(float(v)) for v in a], dtype=np.uint8).reshape(np.shape(x))
+
+
+def cache_write(key, value, in_dt, slot_mapping, kv_cache, kv_dt, *, num_kv_heads, head_dim, page_size,
+                k_scale=1.0, v_scale=1.0):
+    """Write key/value rows [T, Hkv, D] into a copy of kv_cache at slot_mapping; returns the new cache."""
+    ka, code = _storage(key, in_dt)
+    va, _ = _storage(value, in_dt)
+    cache = np.array(kv_cache, copy=True)
+    ca, cc = _storage(cache, kv_dt)
+    sm = _c(slot_mapping, np.int64).reshape(-1)
+    num_pages = ca.size // (int(num_kv_heads) * int(page_size) * 2 * int(head_dim))
+    rc = _load().orc_cache_write(_ptr(ka), _ptr(va), code, _ptr(sm), sm.size, int(num_kv_heads), int(head_dim),
+                                 int(page_size), num_pages, _ptr(ca), cc, float(k_scale), float(v_scale))
+    if rc != 0:
+        raise ValueError(f"cache_write oracle rejected its input (code {rc})")
+    return ca.reshape(np.shape(kv_cache))
+
+
+def segmented_paged(q, dt, kv_cache, block_table, seg_start, used, bias, *, num_kv_heads, page_size, topk, bs,
+                    local, return_segments=False, threads=1):
+    """DASH segmented attention over key ranges of each query's request in a paged cache.
+
+    q: storage [n, Hq, D]; kv_cache: storage [num_pages, Hkv, P, 2D];
+    block_table int32 [n, W]; seg_start, used int32 [n, topk+1]; bias [n, topk].
+    """
+    qa, code = _storage(q, dt)
+    ca, _ = _storage(kv_cache, dt)
+    n, Hq, D = qa.shape
+    bt = _c(block_table, np.int32)
+    ss = _c(seg_start, np.int32).reshape(-1)
+    u = _c(used, np.int32).reshape(-1)
+    bi = _c(bias, np.float64).reshape(-1) if topk > 0 else np.zeros(1, np.float64)
+    num_pages = ca.size // (int(num_kv_heads) * int(page_size) * 2 * D)
+    out = np.zeros((n, Hq, D), np.float64)
+    seg_out = np.zeros((n, topk + 1, Hq, D), np.float64) if return_segments else None
+    seg_lse = np.zeros((n, topk + 1, Hq), np.float64) if return_segments else None
+    rc = _load().orc_segmented_paged(
+        _ptr(qa), code, _ptr(ca), num_pages, _ptr(bt), bt.shape[1], _ptr(ss), _ptr(u), _ptr(bi), n, Hq,
+        int(num_kv_heads), D, int(page_size), int(topk), int(bs), int(local), _ptr(out), _ptr(seg_out),
+        _ptr(seg_lse), int(threads))
+    if rc != 0:
+        raise ValueError(f"segmented_paged oracle rejected its input (code {rc})")
+    return (out, seg_out, seg_lse) if return_segments else out

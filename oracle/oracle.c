@@ -400,3 +400,158 @@ int orc_lse_merge(const double* part_out, const double* part_lse, const double* 
     }
     return 0;
 }
+
+/* ---------------------------------------------------------------------------
+ * KV-cache write [TS FlashInferTSImpl.do_kv_cache_update: reshape_and_cache_flash].
+ *
+ * Token t's key and value rows [Hkv, D] go to slot s = slot_mapping[t] of the
+ * paged cache: page s / P, offset s % P, K into [..., :D] and V into
+ * [..., D:] (the layout _kv_views reads back).  A negative slot is a padding
+ * token and writes nothing.  A 16-bit cache of the input's type stores the
+ * input bits unchanged; an fp8 cache stores e4m3(x / scale) with the key
+ * (value) scale, the quotient taken in fp32 and rounded to nearest even,
+ * saturating to +-448 (the largest finite e4m3fn value).
+ * ------------------------------------------------------------------------- */
+uint8_t orc_encode_e4m3(float x) {
+    if (isnan(x)) return 0x7F;
+    const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs((double)x);
+    if (a >= 448.0) return sign | 0x7E;        /* saturate (and +-inf) */
+    if (a < ldexp(1.0, -6)) {
+        /* subnormal step 2^-9; a result of 8 is the smallest normal, code 0x08 */
+        double t = nearbyint(a * 512.0);
+        return sign | (uint8_t)t;
+    }
+    int k;
+    frexp(a, &k);                               /* a = f * 2^k, f in [0.5, 1) */
+    int e = k - 1;                              /* a = s * 2^e, s in [1, 2) */
+    double t = nearbyint((ldexp(a, -e) - 1.0) * 8.0);
+    if (t >= 8.0) {
+        t = 0.0;
+        e += 1;
+    }
+    if (e > 8 || (e == 8 && t > 6.0)) return sign | 0x7E;  /* 480 and up round to the NaN code: saturate */
+    return sign | (uint8_t)(((e + 7) << 3) | (int)t);
+}
+
+int orc_cache_write(const void* key, const void* value, int in_dt, const int64_t* slot_mapping,
+                    long num_tokens, int Hkv, int D, int P, long num_pages, void* cache, int kv_dt,
+                    float k_scale, float v_scale) {
+    if (Hkv <= 0 || D <= 0 || P <= 0 || num_pages <= 0) return -1;
+    if (kv_dt != ORC_FP8_E4M3 && kv_dt != in_dt) return -1;
+    for (long t = 0; t < num_tokens; ++t) {
+        const int64_t s = slot_mapping[t];
+        if (s < 0) continue;
+        const long page = (long)(s / P), off = (long)(s % P);
+        if (page >= num_pages) return -2;
+        for (int h = 0; h < Hkv; ++h) {
+            const size_t src = ((size_t)t * Hkv + h) * D;
+            const size_t dst = (((size_t)page * Hkv + h) * P + off) * 2 * (size_t)D;
+            for (int d = 0; d < D; ++d) {
+                if (kv_dt == ORC_FP8_E4M3) {
+                    const float kx = (float)orc_load(key, src + d, in_dt);
+                    const float vx = (float)orc_load(value, src + d, in_dt);
+                    ((uint8_t*)cache)[dst + d] = orc_encode_e4m3(kx / k_scale);
+                    ((uint8_t*)cache)[dst + D + d] = orc_encode_e4m3(vx / v_scale);
+                } else {
+                    ((uint16_t*)cache)[dst + d] = ((const uint16_t*)key)[src + d];
+                    ((uint16_t*)cache)[dst + D + d] = ((const uint16_t*)value)[src + d];
+                }
+            }
+        }
+    }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * DASH segmented attention read from the paged cache: segment g of query i is
+ * the key range [seg_start[i, g], seg_start[i, g] + used[i, g]) of request row
+ * i, each key gathered through the block table exactly as paged decode reads
+ * it; attention per segment and the combine are those of
+ * orc_segmented_attention (scale D^-0.5, prior [bias, 0], dead segments out).
+ * ------------------------------------------------------------------------- */
+int orc_segmented_paged(const void* q, int dt, const void* cache, long num_pages, const int32_t* block_table,
+                        long bt_stride, const int32_t* seg_start, const int32_t* used, const double* bias,
+                        int n, int Hq, int Hkv, int D, int P, int topk, int bs, int local, double* out,
+                        double* seg_out, double* seg_lse, int nthreads) {
+    if (n < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || P <= 0 || topk < 0) return -1;
+    if (Hq % Hkv != 0) return -1;
+    const int G = Hq / Hkv;
+    const int groups = topk + 1;
+    const double scale = 1.0 / sqrt((double)D);
+    if (nthreads < 1) nthreads = 1;
+    for (long i = 0; i < (long)n * groups; ++i) {
+        const int cap = (int)(i % groups) < topk ? bs : local;
+        if (used[i] < 0 || used[i] > cap || seg_start[i] < 0) return -3;
+        for (long t = seg_start[i]; t < (long)seg_start[i] + used[i]; ++t) {
+            const long page = block_table[(i / groups) * bt_stride + t / P];
+            if (page < 0 || page >= num_pages) return -2;
+        }
+    }
+
+#pragma omp parallel for collapse(2) schedule(dynamic) num_threads(nthreads)
+    for (int i = 0; i < n; ++i) {
+        for (int h = 0; h < Hq; ++h) {
+            const int hk = h / G;
+            const int cap_max = bs > local ? bs : local;
+            double* s = (double*)malloc(sizeof(double) * (size_t)(cap_max > 0 ? cap_max : 1));
+            double* o = (double*)malloc(sizeof(double) * (size_t)groups * D);
+            double* l = (double*)malloc(sizeof(double) * (size_t)groups);
+            double* qd = (double*)malloc(sizeof(double) * (size_t)D);
+            for (int d = 0; d < D; ++d) qd[d] = orc_load(q, (size_t)(((long)i * Hq + h) * D + d), dt);
+            for (int g = 0; g < groups; ++g) {
+                const long st = seg_start[(long)i * groups + g];
+                const long u = used[(long)i * groups + g];
+                for (long t = 0; t < u; ++t) {
+                    const long j = st + t;
+                    const long page = block_table[(long)i * bt_stride + j / P];
+                    const size_t kbase = (size_t)(((page * Hkv + hk) * P + j % P) * 2L * D);
+                    double dot = 0.0;
+                    for (int d = 0; d < D; ++d) dot += qd[d] * orc_load(cache, kbase + d, dt);
+                    s[t] = scale * dot;
+                }
+                double m;
+                orc_softmax_lse(s, u, &m, &l[g]);
+                for (int d = 0; d < D; ++d) {
+                    double acc = 0.0;
+                    for (long t = 0; t < u; ++t) {
+                        const long j = st + t;
+                        const long page = block_table[(long)i * bt_stride + j / P];
+                        const size_t vbase = (size_t)(((page * Hkv + hk) * P + j % P) * 2L * D + D);
+                        acc += exp(s[t] - l[g]) * orc_load(cache, vbase + d, dt);
+                    }
+                    o[(long)g * D + d] = u > 0 ? acc : 0.0;
+                }
+                if (seg_out)
+                    for (int d = 0; d < D; ++d)
+                        seg_out[(((long)i * groups + g) * Hq + h) * D + d] = o[(long)g * D + d];
+                if (seg_lse) seg_lse[((long)i * groups + g) * Hq + h] = l[g];
+            }
+            double mx = -INFINITY;
+            for (int g = 0; g < groups; ++g) {
+                if (used[(long)i * groups + g] <= 0) continue;
+                const double lg = l[g] + (g < topk ? bias[(long)i * topk + g] : 0.0);
+                if (lg > mx) mx = lg;
+            }
+            double denom = 0.0;
+            for (int g = 0; g < groups; ++g) {
+                if (used[(long)i * groups + g] <= 0) continue;
+                denom += exp(l[g] + (g < topk ? bias[(long)i * topk + g] : 0.0) - mx);
+            }
+            for (int d = 0; d < D; ++d) {
+                double acc = 0.0;
+                for (int g = 0; g < groups; ++g) {
+                    if (used[(long)i * groups + g] <= 0) continue;
+                    acc += exp(l[g] + (g < topk ? bias[(long)i * topk + g] : 0.0) - mx) / denom *
+                           o[(long)g * D + d];
+                }
+                out[((long)i * Hq + h) * D + d] = acc;
+            }
+            free(qd);
+            free(l);
+            free(o);
+            free(s);
+        }
+    }
+    return 0;
+}

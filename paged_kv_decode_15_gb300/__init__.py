@@ -22,11 +22,11 @@ LIB_PATH = os.path.join(_HERE, "libpkd.so")
 
 OK, EINVAL, EUNSUPPORTED, ECUDA, EDEVICE_BOUNDS, ETIMEOUT = range(6)
 BF16, FP16, FP8_E4M3, FP32 = 0, 1, 2, 3
-FLAG_CAUSAL, FLAG_MMA_SMALL_M, FLAG_FMA = 1, 2, 4
+FLAG_CAUSAL, FLAG_MMA_SMALL_M, FLAG_FMA, FLAG_GRID = 1, 2, 4, 8
 
 SYMBOLS = ("pkd_version", "pkd_last_error", "pkd_paged_decode_workspace_size", "pkd_workspace_init",
-           "pkd_workspace_check", "pkd_paged_decode", "pkd_paged_decode_static", "pkd_segmented_attention",
-           "pkd_lse_merge")
+           "pkd_workspace_check", "pkd_paged_decode", "pkd_paged_decode_static", "pkd_cache_write",
+           "pkd_segmented_attention", "pkd_segmented_attention_paged", "pkd_lse_merge")
 
 
 class PkdError(RuntimeError):
@@ -65,10 +65,13 @@ def load_library(path: str = LIB_PATH):
                                      P, I, P, P, SZ, I, U, P]
     lib.pkd_paged_decode_static.argtypes = [P, I, P, I, I64, P, I64, P, I, I, I, I, I, I, I, F, F, F, F, I,
                                             P, I, P, I, U, P]
+    lib.pkd_cache_write.argtypes = [P, P, I, I64, I64, P, I64, I, I, I, I64, P, I, F, F, P]
     lib.pkd_segmented_attention.argtypes = [P, P, P, I, P, P, I, I, I, I, I, I, I, P, P, P, P]
+    lib.pkd_segmented_attention_paged.argtypes = [P, I, P, I64, P, I64, P, P, P, I, I, I, I, I, I, I, I, I,
+                                                  P, P, P, P]
     lib.pkd_lse_merge.argtypes = [P, P, P, P, I, I, I, I, P, I, P, P]
     for name in ("pkd_workspace_init", "pkd_workspace_check", "pkd_paged_decode", "pkd_paged_decode_static",
-                 "pkd_segmented_attention", "pkd_lse_merge"):
+                 "pkd_cache_write", "pkd_segmented_attention", "pkd_segmented_attention_paged", "pkd_lse_merge"):
         getattr(lib, name).restype = I
     _lib = lib
     return lib
@@ -144,7 +147,7 @@ def _workspace(nbytes: int, device) -> torch.Tensor:
 
 def paged_decode(q, kv_cache, block_table, seq_lens, scale, window=0, out=None, lse=None, *, q_scale=1.0,
                  k_scale=1.0, v_scale=1.0, max_kv_len=None, workspace=None, chunk_tokens=0, causal=False,
-                 mma_small_m=False, force_fma=False, out_dtype=None, stream=None):
+                 mma_small_m=False, force_fma=False, grid=False, out_dtype=None, stream=None):
     """Attention of each request's query block over its paged keys.
 
     q [B, sq, Hq, D]; kv_cache [num_pages, Hkv, P, 2*D] (bf16, fp16, or uint8 /
@@ -174,7 +177,8 @@ def paged_decode(q, kv_cache, block_table, seq_lens, scale, window=0, out=None, 
         lse = torch.empty((B, sq, Hq), dtype=torch.float32, device=q.device)
     if max_kv_len is None:
         max_kv_len = block_table.shape[1] * P
-    flags = (FLAG_CAUSAL if causal else 0) | (FLAG_MMA_SMALL_M if mma_small_m else 0) | (FLAG_FMA if force_fma else 0)
+    flags = (FLAG_CAUSAL if causal else 0) | (FLAG_MMA_SMALL_M if mma_small_m else 0) | \
+        (FLAG_FMA if force_fma else 0) | (FLAG_GRID if grid else 0)
     need = workspace_size(B, sq, Hq, Hkv, D, P, max_kv_len, kv_dt, window, chunk_tokens, flags)
     if workspace is None:
         workspace = _workspace(need, q.device)
@@ -215,6 +219,37 @@ def segmented_attention(q, k, v, used, bias, bs, local, out=None, *, seg_out=Non
     return (out, seg_out, seg_lse) if return_segments else out
 
 
+def segmented_attention_paged(q, kv_cache, block_table, seg_start, used, bias, bs, local, out=None, *,
+                              max_kv_len=None, return_segments=False, stream=None):
+    """DASH segmented attention over key ranges of each query's request in a paged cache.
+
+    q [n, Hq, D]; kv_cache [num_pages, Hkv, P, 2D]; block_table int32 [n, W];
+    seg_start, used int32 [n, topk+1]; bias fp32 [n, topk].
+    """
+    lib = load_library()
+    n, Hq, D = q.shape
+    num_pages, Hkv, P, _ = kv_cache.shape
+    topk = bias.shape[1] if bias is not None else 0
+    for t, name in ((q, "q"), (kv_cache, "kv_cache"), (block_table, "block_table"), (seg_start, "seg_start"),
+                    (used, "used"), (bias, "bias")):
+        _cuda(t, name)
+        if t is not None and not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if out is None:
+        out = torch.empty_like(q)
+    seg_out = seg_lse = None
+    if return_segments:
+        seg_out = torch.empty((n, topk + 1, Hq, D), dtype=torch.float32, device=q.device)
+        seg_lse = torch.empty((n, topk + 1, Hq), dtype=torch.float32, device=q.device)
+    if max_kv_len is None:
+        max_kv_len = block_table.shape[1] * P
+    _check(lib.pkd_segmented_attention_paged(
+        _ptr(q), dtype_code(q.dtype), _ptr(kv_cache), num_pages, _ptr(block_table), block_table.stride(0),
+        _ptr(seg_start), _ptr(used), _ptr(bias), n, Hq, Hkv, D, P, topk, int(bs), int(local), int(max_kv_len),
+        _ptr(out), _ptr(seg_out), _ptr(seg_lse), _stream(stream)))
+    return (out, seg_out, seg_lse) if return_segments else out
+
+
 def lse_merge(part_out, part_lse, prior=None, live=None, out=None, lse_out=None, out_dtype=torch.float32,
               stream=None):
     """Merge partials part_out [N, S, H, D] fp32 by their LSE [N, S, H]."""
@@ -231,3 +266,23 @@ def lse_merge(part_out, part_lse, prior=None, live=None, out=None, lse_out=None,
     _check(lib.pkd_lse_merge(_ptr(part_out), _ptr(part_lse), _ptr(prior), _ptr(live), N, S, H, D, _ptr(out),
                              dtype_code(out.dtype), _ptr(lse_out), _stream(stream)))
     return out, lse_out
+
+
+def cache_write(key, value, slot_mapping, kv_cache, k_scale=1.0, v_scale=1.0, stream=None):
+    """Write key/value rows [T, Hkv, D] (bf16/fp16) into their slots of kv_cache
+    [num_pages, Hkv, P, 2D] (same dtype, or uint8 / float8_e4m3fn for fp8)."""
+    lib = load_library()
+    for t, n in ((key, "key"), (value, "value"), (slot_mapping, "slot_mapping"), (kv_cache, "kv_cache")):
+        _cuda(t, n)
+    T, Hkv, D = key.shape
+    num_pages, Hkv2, P, twoD = kv_cache.shape
+    if Hkv2 != Hkv or twoD != 2 * D:
+        raise ValueError("kv_cache shape does not match key")
+    if slot_mapping.dtype != torch.int64:
+        raise TypeError("slot_mapping must be int64")
+    if key.stride(2) != 1 or key.stride(1) != D or value.stride(2) != 1 or value.stride(1) != D:
+        raise ValueError("rows of one token must be contiguous")
+    _check(lib.pkd_cache_write(_ptr(key), _ptr(value), dtype_code(key.dtype), key.stride(0), value.stride(0),
+                               _ptr(slot_mapping), T, Hkv, D, P, num_pages, _ptr(kv_cache), dtype_code(kv_cache.dtype),
+                               float(k_scale), float(v_scale), _stream(stream)))
+    return kv_cache

@@ -46,6 +46,7 @@ constexpr size_t kHeader = 256;    // workspace status word lives in the first b
 
 struct Plan {
     bool mma;
+    bool flat;
     int M, G;
     int mt, nt;    // tensor-core tiles
     int lpt, mr;   // CUDA-core lanes per key, padded rows
@@ -68,14 +69,18 @@ pkd_status make_plan(int B, int sq, int Hq, int Hkv, int D, int P, int max_kv_le
     pl.G = Hq / Hkv;
     pl.M = sq * pl.G;
     const int M = pl.M;
-    if (kv == PKD_FP8_E4M3) {
-        if (M > 8) return fail(PKD_EUNSUPPORTED, "fp8 caches support sq*num_heads/num_kv_heads <= 8 (got %d)", M);
+    pl.flat = B <= pkd::kFlatMaxBatch && !(flags & PKD_FLAG_GRID);
+    if (kv == PKD_FP8_E4M3 && (!pl.flat || (flags & PKD_FLAG_FMA))) {
+        // the chunked grid reads fp8 on CUDA cores only
+        if (M > 8) return fail(PKD_EUNSUPPORTED, "fp8 on CUDA cores supports sq*num_heads/num_kv_heads <= 8 (got %d)", M);
         pl.mma = false;
     } else if (flags & PKD_FLAG_FMA) {
         if (M > 8) return fail(PKD_EUNSUPPORTED, "the CUDA-core kernel supports sq*num_heads/num_kv_heads <= 8 (got %d)", M);
         pl.mma = false;
     } else {
-        pl.mma = M > 8 || (flags & PKD_FLAG_MMA_SMALL_M);
+        // 16-bit caches use the tensor-core kernel at every M (measured faster
+        // than CUDA cores also for M < 16); PKD_FLAG_FMA selects CUDA cores.
+        pl.mma = true;
     }
     if (pl.mma) {
         if (M > 32) return fail(PKD_EUNSUPPORTED, "sq*num_heads/num_kv_heads = %d > 32", M);
@@ -110,7 +115,9 @@ pkd_status make_plan(int B, int sq, int Hq, int Hkv, int D, int P, int max_kv_le
     pl.max_splits = pl.max_vis > 0 ? (pl.max_vis + pl.chunk - 1) / pl.chunk : 1;
     pl.off_counters = kHeader;
     pl.off_lse = pl.off_counters + round_up((size_t)units * 4, 256);
-    const size_t parts = (size_t)units * pl.max_splits;
+    // partial results: per (unit, chunk) for the chunked grid, per (warp, side)
+    // for the flat partition
+    const size_t parts = pl.flat ? (size_t)pkd::kFlatMaxWorkers * 2 : (size_t)units * pl.max_splits;
     pl.off_out = pl.off_lse + round_up(parts * M * 4, 256);
     pl.bytes = pl.off_out + round_up(parts * M * D * 4, 256);
     return PKD_OK;
@@ -186,6 +193,47 @@ pkd_status get_map(CUtensorMap& out, const void* base, int rank, uint64_t d0, ui
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(PKD_ECUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+    {
+        std::lock_guard<std::mutex> g(c.mu);
+        const int slot = c.used < MapCache::N ? c.used++ : (c.next++ % MapCache::N);
+        c.key[slot] = k;
+        c.map[slot] = m;
+    }
+    out = m;
+    return PKD_OK;
+}
+
+// The "stage map" of a paged cache: {128-byte chunk, key row, chunk of the
+// row}, strides {row bytes, 128 B}, box {one chunk, 16 rows, every chunk},
+// so one TMA copy loads a 16-key stage (K and V) chunk-major.
+pkd_status get_stage_map(CUtensorMap& out, const void* cache, uint64_t rows, int row_bytes, pkd_dtype dt) {
+    const int elt = elt_bytes(dt);
+    MapKey k;
+    std::memset(&k, 0, sizeof k);
+    k.base = cache; k.d0 = 128 / elt; k.d1 = rows; k.d2 = row_bytes / 128; k.s1 = row_bytes; k.s2 = 128;
+    k.rank = 103; k.dtype = dt;
+    MapCache& c = map_cache();
+    {
+        std::lock_guard<std::mutex> g(c.mu);
+        for (int i = 0; i < c.used; ++i)
+            if (c.key[i] == k) {
+                out = c.map[i];
+                return PKD_OK;
+            }
+    }
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return fail(PKD_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const CUtensorMapDataType t = dt == PKD_BF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                  : dt == PKD_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                   : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    cuuint64_t dims[3] = {k.d0, k.d1, k.d2};
+    cuuint64_t strides[2] = {k.s1, k.s2};
+    cuuint32_t box[3] = {(cuuint32_t)(128 / elt), (cuuint32_t)pkd::kStageTok, (cuuint32_t)(row_bytes / 128)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUtensorMap m;
+    CUresult r = enc(&m, t, 3, const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PKD_ECUDA, "cuTensorMapEncodeTiled (stage map) failed (CUresult %d)", (int)r);
     {
         std::lock_guard<std::mutex> g(c.mu);
         const int slot = c.used < MapCache::N ? c.used++ : (c.next++ % MapCache::N);
@@ -281,7 +329,7 @@ pkd_status pkd_paged_decode(const void* q, pkd_dtype q_dtype, const void* kv_cac
     CUtensorMap tmap;
     const int elt = elt_bytes(kv_dtype);
     const uint64_t rows = (uint64_t)num_pages * num_kv_heads * page_size;
-    st = get_map(tmap, kv_cache, 2, 2ull * head_dim, rows, 0, 2ull * head_dim * elt, 0, kv_dtype, pkd::kStageTok);
+    st = get_stage_map(tmap, kv_cache, rows, 2 * head_dim * elt, kv_dtype);
     if (st != PKD_OK) return st;
 
     pkd::DecodeParams p;
@@ -314,14 +362,52 @@ pkd_status pkd_paged_decode(const void* q, pkd_dtype q_dtype, const void* kv_cac
     p.scale_log2 = scale * q_scale * k_scale * pkd::kLog2e;
     p.v_scale = v_scale;
 
-    const dim3 grid(pl.max_splits, num_kv_heads, batch);
     cudaError_t e;
-    if (pl.mma)
-        e = pkd::launch_decode_mma(head_dim, kv_dtype == PKD_BF16, pl.mt, pl.nt, tmap, p, grid, (cudaStream_t)stream);
+    cudaStream_t s = (cudaStream_t)stream;
+    const int max_ctas = pkd::kFlatMaxWorkers / pkd::kNW;
+    if (pl.flat && pl.mma)
+        e = kv_dtype == PKD_BF16   ? pkd::launch_flat_mma_bf16(head_dim, pl.mt, pl.nt, tmap, p, max_ctas, s)
+            : kv_dtype == PKD_FP16 ? pkd::launch_flat_mma_fp16(head_dim, pl.mt, pl.nt, tmap, p, max_ctas, s)
+                                   : pkd::launch_flat_mma_fp8(head_dim, pl.mt, pl.nt, tmap, p, max_ctas, s);
+    else if (pl.flat)
+        e = kv_dtype == PKD_BF16   ? pkd::launch_flat_fma_bf16(head_dim, pl.lpt, pl.mr, tmap, p, max_ctas, s)
+            : kv_dtype == PKD_FP16 ? pkd::launch_flat_fma_fp16(head_dim, pl.lpt, pl.mr, tmap, p, max_ctas, s)
+                                   : pkd::launch_flat_fma_fp8(head_dim, pl.lpt, pl.mr, tmap, p, max_ctas, s);
+    else if (pl.mma)
+        e = pkd::launch_decode_mma(head_dim, kv_dtype == PKD_BF16, pl.mt, pl.nt, tmap, p,
+                                   dim3(pl.max_splits, num_kv_heads, batch), s);
     else
-        e = pkd::launch_decode_fma(head_dim, (int)kv_dtype, pl.lpt, pl.mr, tmap, p, grid, (cudaStream_t)stream);
+        e = pkd::launch_decode_fma(head_dim, (int)kv_dtype, pl.lpt, pl.mr, tmap, p,
+                                   dim3(pl.max_splits, num_kv_heads, batch), s);
     if (e != cudaSuccess) return cuda_fail(e, "pkd_paged_decode launch");
     return PKD_OK;
+}
+
+pkd_status pkd_cache_write(const void* key, const void* value, pkd_dtype in_dtype, int64_t key_stride,
+                           int64_t value_stride, const int64_t* slot_mapping, int64_t num_tokens, int num_kv_heads,
+                           int head_dim, int page_size, int64_t num_pages, void* kv_cache, pkd_dtype kv_dtype,
+                           float k_scale, float v_scale, void* stream) {
+    if (num_tokens < 0 || num_kv_heads < 1 || page_size < 1 || num_pages < 1)
+        return fail(PKD_EINVAL, "invalid shape: num_tokens=%lld num_kv_heads=%d page_size=%d num_pages=%lld",
+                    (long long)num_tokens, num_kv_heads, page_size, (long long)num_pages);
+    if (head_dim != 64 && head_dim != 128) return fail(PKD_EUNSUPPORTED, "head_dim %d not supported", head_dim);
+    if (in_dtype != PKD_BF16 && in_dtype != PKD_FP16)
+        return fail(PKD_EUNSUPPORTED, "key/value dtype %d not supported (bf16, fp16)", (int)in_dtype);
+    if (kv_dtype != in_dtype && kv_dtype != PKD_FP8_E4M3)
+        return fail(PKD_EUNSUPPORTED, "cache dtype %d must equal the input dtype or be fp8-e4m3", (int)kv_dtype);
+    if (key_stride < (int64_t)num_kv_heads * head_dim || value_stride < (int64_t)num_kv_heads * head_dim ||
+        key_stride % 8 || value_stride % 8)
+        return fail(PKD_EINVAL, "token strides must be >= num_kv_heads*head_dim and multiples of 8 elements");
+    if (kv_dtype == PKD_FP8_E4M3 && (!(k_scale > 0.f) || !(v_scale > 0.f)))
+        return fail(PKD_EINVAL, "fp8 scales must be positive");
+    if (num_tokens == 0) return PKD_OK;
+    if (!key || !value || !slot_mapping || !kv_cache) return fail(PKD_EINVAL, "null pointer argument");
+    if (!aligned(key, 16) || !aligned(value, 16) || !aligned(kv_cache, 16) || !aligned(slot_mapping, 8))
+        return fail(PKD_EINVAL, "key, value and kv_cache must be 16-byte aligned");
+    cudaError_t e = pkd::launch_cache_write(key, value, (int)in_dtype, slot_mapping, num_tokens, key_stride,
+                                            value_stride, num_kv_heads, head_dim, page_size, num_pages, kv_cache,
+                                            (int)kv_dtype, k_scale, v_scale, (cudaStream_t)stream);
+    return e == cudaSuccess ? PKD_OK : cuda_fail(e, "pkd_cache_write launch");
 }
 
 pkd_status pkd_segmented_attention(const void* q, const void* k, const void* v, pkd_dtype dtype, const int32_t* used,
@@ -377,6 +463,72 @@ pkd_status pkd_segmented_attention(const void* q, const void* k, const void* v, 
     p.scale_log2 = pkd::kLog2e / sqrtf((float)head_dim);
     cudaError_t e = pkd::launch_segmented(p, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "pkd_segmented_attention launch");
+    return PKD_OK;
+}
+
+pkd_status pkd_segmented_attention_paged(const void* q, pkd_dtype dtype, const void* kv_cache, int64_t num_pages,
+                                         const int32_t* block_table, int64_t block_table_stride,
+                                         const int32_t* seg_start, const int32_t* used, const float* bias, int n,
+                                         int num_heads, int num_kv_heads, int head_dim, int page_size, int topk,
+                                         int bs, int local, int max_kv_len, void* out, float* seg_out,
+                                         float* seg_lse, void* stream) {
+    if (n < 0 || num_heads < 1 || num_kv_heads < 1 || topk < 0 || bs < 0 || local < 0 || max_kv_len < 0 ||
+        num_pages < 1 || page_size < 1)
+        return fail(PKD_EINVAL, "invalid shape: n=%d num_heads=%d num_kv_heads=%d topk=%d bs=%d local=%d", n,
+                    num_heads, num_kv_heads, topk, bs, local);
+    if (dtype != PKD_BF16 && dtype != PKD_FP16)
+        return fail(PKD_EUNSUPPORTED, "segmented attention needs fp16 or bf16 (got dtype %d)", (int)dtype);
+    if (head_dim != 64 && head_dim != 128) return fail(PKD_EUNSUPPORTED, "head_dim %d not supported", head_dim);
+    if (page_size % 16) return fail(PKD_EUNSUPPORTED, "page_size %d must be a multiple of 16", page_size);
+    if (num_heads % num_kv_heads) return fail(PKD_EUNSUPPORTED, "num_heads must be a multiple of num_kv_heads");
+    const int G = num_heads / num_kv_heads;
+    if (G > 16) return fail(PKD_EUNSUPPORTED, "num_heads/num_kv_heads = %d > 16", G);
+    if (topk + 1 > 64) return fail(PKD_EUNSUPPORTED, "topk must be < 64");
+    const long long stages = (long long)topk * ((bs + 15) / 16 + 1) + (local + 15) / 16 + 1;
+    if (stages > 512) return fail(PKD_EUNSUPPORTED, "segments span more than 512 16-key stages per query");
+    if ((seg_out == nullptr) != (seg_lse == nullptr))
+        return fail(PKD_EINVAL, "seg_out and seg_lse must be given together");
+    if (block_table_stride < ((int64_t)max_kv_len + page_size - 1) / page_size)
+        return fail(PKD_EINVAL, "block_table_stride < ceil(max_kv_len/page_size)");
+    if ((int64_t)num_pages * num_kv_heads * page_size >= (int64_t)1 << 31)
+        return fail(PKD_EUNSUPPORTED, "cache too large");
+    if (n == 0) return PKD_OK;
+    if (!q || !kv_cache || !block_table || !seg_start || !used || !out || (topk > 0 && !bias))
+        return fail(PKD_EINVAL, "null pointer argument");
+    if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16))
+        return fail(PKD_EINVAL, "q, kv_cache and out must be 16-byte aligned");
+
+    pkd::SegmentParams p;
+    std::memset(&p, 0, sizeof p);
+    const uint64_t rows = (uint64_t)num_pages * num_kv_heads * page_size;
+    pkd_status st = get_stage_map(p.kmap, kv_cache, rows, 4 * head_dim, dtype);
+    if (st != PKD_OK) return st;
+    p.vmap = p.kmap;
+    p.paged = 1;
+    p.block_table = block_table;
+    p.bt_stride = block_table_stride;
+    p.seg_start = seg_start;
+    p.num_pages = num_pages;
+    p.P = page_size;
+    p.max_kv_len = max_kv_len;
+    p.q = q;
+    p.used = used;
+    p.bias = bias;
+    p.out = out;
+    p.seg_out = seg_out;
+    p.seg_lse = seg_lse;
+    p.n = n;
+    p.Hq = num_heads;
+    p.Hkv = num_kv_heads;
+    p.G = G;
+    p.D = head_dim;
+    p.topk = topk;
+    p.bs = bs;
+    p.local = local;
+    p.bf16 = dtype == PKD_BF16;
+    p.scale_log2 = pkd::kLog2e / sqrtf((float)head_dim);
+    cudaError_t e = pkd::launch_segmented(p, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "pkd_segmented_attention_paged launch");
     return PKD_OK;
 }
 

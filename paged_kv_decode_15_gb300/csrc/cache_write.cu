@@ -1,0 +1,109 @@
+// KV-cache write: new key/value rows into their slots of the paged cache,
+// quantised to e4m3 for an fp8 cache.
+//
+// Each warp moves kItemsPerWarp (token, kv head) rows; lanes 0-15 move key
+// rows, lanes 16-31 value rows, 16 input bytes each, all loads issued first.  A 16-bit cache receives the input bits; an
+// fp8 cache receives e4m3(x / scale) rounded to nearest even with saturation
+// (cvt.rn.satfinite), the quotient an IEEE fp32 division.
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace pkd {
+
+struct CacheWriteParams {
+    const uint8_t* key;     // [T, Hkv, D] rows, token stride key_stride elements
+    const uint8_t* value;
+    const int64_t* slots;   // [T]
+    uint8_t* cache;         // [num_pages, Hkv, P, 2D]
+    long long T, key_stride, value_stride, num_pages;
+    int Hkv, D, P, in_elt, kv_elt, in_bf16;
+    float k_scale, v_scale;
+};
+
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+constexpr int kItemsPerWarp = 4;  // (token, kv head) rows per warp, loaded before any is stored
+
+__global__ void __launch_bounds__(128) cache_write_kernel(const CacheWriteParams p) {
+    const long long w0 = (static_cast<long long>(blockIdx.x) * 4 + (threadIdx.x >> 5)) * kItemsPerWarp;
+    const int lane = threadIdx.x & 31;
+    const int part = lane >> 4, c = lane & 15;  // part 0: key, 1: value; 16-byte input chunk c
+    const int chunks = p.D * p.in_elt / 16;
+    const long long total = p.T * p.Hkv;
+    uint4 v[kItemsPerWarp];
+    uint8_t* dst[kItemsPerWarp];
+#pragma unroll
+    for (int it = 0; it < kItemsPerWarp; ++it) {
+        dst[it] = nullptr;
+        const long long wid = w0 + it;
+        if (wid >= total || c >= chunks) continue;
+        const long long t = wid / p.Hkv;
+        const int h = static_cast<int>(wid % p.Hkv);
+        const long long s = p.slots[t];
+        if (s < 0 || s / p.P >= p.num_pages) continue;
+        const long long page = s / p.P, off = s % p.P;
+        const uint8_t* src = (part ? p.value + (t * p.value_stride + static_cast<long long>(h) * p.D) * p.in_elt
+                                   : p.key + (t * p.key_stride + static_cast<long long>(h) * p.D) * p.in_elt) +
+                             c * 16;
+        v[it] = __ldg(reinterpret_cast<const uint4*>(src));
+        dst[it] = p.cache + (((page * p.Hkv + h) * p.P + off) * 2 * p.D + part * p.D) * p.kv_elt;
+    }
+    const float scale = part ? p.v_scale : p.k_scale;
+#pragma unroll
+    for (int it = 0; it < kItemsPerWarp; ++it) {
+        if (!dst[it]) continue;
+        if (p.kv_elt == 2) {
+            *reinterpret_cast<uint4*>(dst[it] + c * 16) = v[it];
+            continue;
+        }
+        const uint32_t w[4] = {v[it].x, v[it].y, v[it].z, v[it].w};
+        uint32_t out[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            float f[4];
+            if (p.in_bf16) {
+                bf16x2_to_f32(w[2 * i], f[0], f[1]);
+                bf16x2_to_f32(w[2 * i + 1], f[2], f[3]);
+            } else {
+                f16x2_to_f32(w[2 * i], f[0], f[1]);
+                f16x2_to_f32(w[2 * i + 1], f[2], f[3]);
+            }
+            out[i] = f32x2_to_e4m3x2(__fdiv_rn(f[0], scale), __fdiv_rn(f[1], scale)) |
+                     (f32x2_to_e4m3x2(__fdiv_rn(f[2], scale), __fdiv_rn(f[3], scale)) << 16);
+        }
+        *reinterpret_cast<uint2*>(dst[it] + c * 8) = make_uint2(out[0], out[1]);
+    }
+}
+
+cudaError_t launch_cache_write(const void* key, const void* value, int in_dtype, const int64_t* slots,
+                               long long T, long long key_stride, long long value_stride, int Hkv, int D, int P,
+                               long long num_pages, void* cache, int kv_dtype, float k_scale, float v_scale,
+                               cudaStream_t stream) {
+    CacheWriteParams p;
+    p.key = static_cast<const uint8_t*>(key);
+    p.value = static_cast<const uint8_t*>(value);
+    p.slots = slots;
+    p.cache = static_cast<uint8_t*>(cache);
+    p.T = T;
+    p.key_stride = key_stride;
+    p.value_stride = value_stride;
+    p.num_pages = num_pages;
+    p.Hkv = Hkv;
+    p.D = D;
+    p.P = P;
+    p.in_elt = 2;
+    p.kv_elt = kv_dtype == 2 ? 1 : 2;
+    p.in_bf16 = in_dtype == 0;
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
+    const long long warps = (T * Hkv + kItemsPerWarp - 1) / kItemsPerWarp;
+    if (warps == 0) return cudaSuccess;
+    cache_write_kernel<<<static_cast<unsigned>((warps + 3) / 4), 128, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace pkd

@@ -11,6 +11,11 @@ namespace pkd {
 constexpr int kNW = 4;          // consumer warps per CTA (one warp group)
 constexpr int kStageTok = 16;   // keys per pipeline stage (one TMA box height)
 constexpr int kMaxCtaPages = 256;
+// Stages a warp asks L2 to fetch beyond its shared-memory ring: DRAM latency
+// is covered by L2-resident data instead of more shared memory.
+constexpr int kPrefetch = 4;
+constexpr int kFlatMaxBatch = 1024;    // the flat kernel keeps per-request tables in shared memory
+constexpr int kFlatMaxWorkers = 2048;  // and two partial slots per warp in the workspace
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kLog2e = 1.44269504088896340736f;
 
@@ -137,7 +142,9 @@ __device__ __forceinline__ void load_cta_pages(const DecodeParams& p, const CtaW
     }
 }
 
-// Issue the TMA loads of one 16-key stage: K boxes then V boxes, all
+// Issue the TMA load of one 16-key stage.  The stage map views the cache as
+// {128-byte chunk, key row, chunk index}: one copy brings 16 key rows and lands
+// them chunk-major -- K boxes, then V boxes, 2 KiB each, 128-byte swizzled --
 // completing on `bar`.  A skipped page only arrives on the barrier.
 template <int D, int ELT>
 __device__ __forceinline__ void issue_stage(const CUtensorMap* tmap, const DecodeParams& p,
@@ -154,11 +161,18 @@ __device__ __forceinline__ void issue_stage(const CUtensorMap* tmap, const Decod
     }
     const int row = (pg * p.Hkv + w.hk) * p.P + (tok % p.P);
     mbar_arrive_expect_tx(bar, 2 * HALF);
-#pragma unroll
-    for (int bx = 0; bx < KBOX; ++bx) tma_load_2d(buf + bx * 2048, tmap, bx * (128 / ELT), row, bar, policy);
-#pragma unroll
-    for (int bx = 0; bx < KBOX; ++bx)
-        tma_load_2d(buf + HALF + bx * 2048, tmap, (ROWB + bx * 128) / ELT, row, bar, policy);
+    tma_load_3d(buf, tmap, 0, row, 0, bar, policy);  // the whole 16-key stage in one copy
+}
+
+// L2 prefetch of a stage this CTA will load later (no-op past its keys or
+// for a skipped page).
+__device__ __forceinline__ void prefetch_stage(const CUtensorMap* tmap, const DecodeParams& p, const CtaWork& w,
+                                               const int* pages, int stage) {
+    const int tok = w.t0 + stage * kStageTok;
+    if (tok >= w.t1) return;
+    const int pg = pages[(tok - w.t0) / p.P];
+    if (pg < 0) return;
+    tma_prefetch_3d(tmap, 0, (pg * p.Hkv + w.hk) * p.P + (tok % p.P), 0);
 }
 
 // Zero the V rows [nvalid, 16) of a stage so that masked keys (past the

@@ -87,6 +87,8 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p
     const uint32_t bar0 = smem_u32(bars + warp * NBUF);
     const uint64_t pol = policy_evict_first();
     if (lane == 0)
+        for (int k = NBUF; k < NBUF + kPrefetch; ++k) prefetch_stage(&tmap, p, w, pages, warp + k * kNW);
+    if (lane == 0)
         for (int k = 0; k < NBUF && k < my_n; ++k)
             issue_stage<D, 2>(&tmap, p, w, pages, warp + k * kNW, ring + k * S::STAGE, bar0 + 8 * k, pol);
 
@@ -109,10 +111,11 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p
         if (pages[(tok0 - w.t0) / p.P] < 0) nvalid = 0;
         const uint32_t st = ring + buf * S::STAGE;
         if (nvalid < kStageTok) zero_tail_v<D, 2>(ring_gen + buf * S::STAGE, nvalid, lane);
-        wp.consume(st, S::HALF, nvalid, p.scale_log2, 0.f,
+        wp.consume(st, S::HALF, nvalid, nvalid < kStageTok || p.causal, p.scale_log2, 0.f,
                    [&](int row, int kt) { return row_sees(p, L, row, tok0 + kt); }, lane);
         __syncwarp();
         if (lane == 0 && k + NBUF < my_n) {
+            prefetch_stage(&tmap, p, w, pages, warp + (k + NBUF + kPrefetch) * kNW);
             fence_proxy_async();
             issue_stage<D, 2>(&tmap, p, w, pages, warp + (k + NBUF) * kNW, st, bar0 + 8 * buf, pol);
         }

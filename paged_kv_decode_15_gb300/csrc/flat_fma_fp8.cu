@@ -1,0 +1,17 @@
+// Flat-partition decode, CUDA-core warps, fp8 caches.
+#include "flat_launch.cuh"
+
+namespace pkd {
+
+cudaError_t launch_flat_fma_fp8(int D, int LPT, int MR, const CUtensorMap& tmap, const DecodeParams& p, int max_ctas,
+                                 cudaStream_t stream) {
+#define PKD_CASE(d, l, m) \
+    if (D == d && LPT == l && MR == m) \
+        return launch_flat_one<FmaWarp<d, 2, l, m>, d, KvType<2>::ELT>(tmap, p, max_ctas, stream);
+    PKD_CASE(128, 8, 2) PKD_CASE(128, 8, 4) PKD_CASE(128, 16, 8)
+    
+#undef PKD_CASE
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace pkd

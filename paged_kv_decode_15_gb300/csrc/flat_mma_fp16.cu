@@ -1,0 +1,16 @@
+// Flat-partition decode, tensor-core warps, fp16 caches.
+#include "flat_launch.cuh"
+
+namespace pkd {
+
+cudaError_t launch_flat_mma_fp16(int D, int MT, int NT, const CUtensorMap& tmap, const DecodeParams& p, int max_ctas,
+                                cudaStream_t stream) {
+#define PKD_CASE(d, mt, nt) \
+    if (D == d && MT == mt && NT == nt) return launch_flat_one<MmaWarp<d, false, mt, nt>, d, 2>(tmap, p, max_ctas, stream);
+    PKD_CASE(128, 1, 1) PKD_CASE(128, 1, 2) PKD_CASE(128, 2, 3) PKD_CASE(128, 2, 4)
+    PKD_CASE(64, 1, 1) PKD_CASE(64, 1, 2) PKD_CASE(64, 2, 3) PKD_CASE(64, 2, 4)
+#undef PKD_CASE
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace pkd

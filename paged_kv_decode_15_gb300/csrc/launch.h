@@ -21,12 +21,32 @@ cudaError_t launch_decode_mma(int D, bool bf16, int MT, int NT, const CUtensorMa
 cudaError_t launch_decode_fma(int D, int kvt, int LPT, int MR, const CUtensorMap& tmap,
                               const DecodeParams& p, dim3 grid, cudaStream_t stream);
 
+// Persistent flat-partition decode: the grid fills the GPU once (at most
+// max_ctas CTAs, one partial slot pair per warp in the workspace).
+cudaError_t launch_flat_mma_bf16(int D, int MT, int NT, const CUtensorMap& tmap, const DecodeParams& p,
+                                 int max_ctas, cudaStream_t stream);
+cudaError_t launch_flat_mma_fp16(int D, int MT, int NT, const CUtensorMap& tmap, const DecodeParams& p,
+                                 int max_ctas, cudaStream_t stream);
+cudaError_t launch_flat_mma_fp8(int D, int MT, int NT, const CUtensorMap& tmap, const DecodeParams& p,
+                                int max_ctas, cudaStream_t stream);
+cudaError_t launch_flat_fma_bf16(int D, int LPT, int MR, const CUtensorMap& tmap, const DecodeParams& p,
+                                 int max_ctas, cudaStream_t stream);
+cudaError_t launch_flat_fma_fp16(int D, int LPT, int MR, const CUtensorMap& tmap, const DecodeParams& p,
+                                 int max_ctas, cudaStream_t stream);
+cudaError_t launch_flat_fma_fp8(int D, int LPT, int MR, const CUtensorMap& tmap, const DecodeParams& p,
+                                int max_ctas, cudaStream_t stream);
+
 // Record `fmt` as this thread's last error message and return `st`.
 int report_status(int st, const char* fmt, ...);
 template <class... A>
 inline pkd_status report(pkd_status st, const char* fmt, A... a) {
     return static_cast<pkd_status>(report_status(static_cast<int>(st), fmt, a...));
 }
+
+cudaError_t launch_cache_write(const void* key, const void* value, int in_dtype, const int64_t* slots,
+                               long long T, long long key_stride, long long value_stride, int Hkv, int D, int P,
+                               long long num_pages, void* cache, int kv_dtype, float k_scale, float v_scale,
+                               cudaStream_t stream);
 
 struct SegmentParams;
 struct MergeParams;

@@ -15,12 +15,36 @@ namespace pkd {
 
 template <int D, bool kBF16, int MT, int NT>
 struct MmaWarp {
-    uint32_t qa[MT][D / 16][4];
+    // With two row tiles the Q fragments would not fit in registers next to
+    // the accumulators: they are then staged in shared memory and re-read.
+    static constexpr bool kQSmem = MT > 1;
+    static constexpr int QSTRIDE = D * 2 + 16;  // bytes per staged q row (conflict-free ldmatrix)
+    uint32_t qa[kQSmem ? 1 : MT][D / 16][4];
+    uint32_t qs = 0;
+    uint8_t* qs_gen = nullptr;
     float m_run[MT][2], l_run[MT][2];
     float oacc[D / 16][NT][4];
 
+    // A fragment of Q for row tile mt, k-step kk
+    __device__ __forceinline__ void q_frag(int mt, int kk, uint32_t (&a)[4], int lane) const {
+        if constexpr (kQSmem) {
+            const int mi = lane >> 3, ri = lane & 7;
+            const int row = mt * 16 + (mi & 1) * 8 + ri;
+            ldsm_x4(qs + row * QSTRIDE + (2 * kk + (mi >> 1)) * 16, a[0], a[1], a[2], a[3]);
+        } else {
+            a[0] = qa[mt][kk][0];
+            a[1] = qa[mt][kk][1];
+            a[2] = qa[mt][kk][2];
+            a[3] = qa[mt][kk][3];
+        }
+    }
+
     // Q fragments from rows staged in shared memory (row stride qstride bytes).
-    __device__ __forceinline__ void load_q(uint32_t qs, int qstride, int lane) {
+    __device__ __forceinline__ void load_q(uint32_t qsm, int qstride, int lane) {
+        if constexpr (kQSmem) {
+            qs = qsm;  // re-read at every stage; the caller keeps the rows in place
+            return;
+        }
         const int mi = lane >> 3, ri = lane & 7;
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
@@ -28,8 +52,67 @@ struct MmaWarp {
             for (int kk = 0; kk < D / 16; ++kk) {
                 const int row = mt * 16 + (mi & 1) * 8 + ri;
                 const int chunk = 2 * kk + (mi >> 1);
-                ldsm_x4(qs + row * qstride + chunk * 16, qa[mt][kk][0], qa[mt][kk][1], qa[mt][kk][2],
+                ldsm_x4(qsm + row * qstride + chunk * 16, qa[mt][kk][0], qa[mt][kk][1], qa[mt][kk][2],
                         qa[mt][kk][3]);
+            }
+    }
+
+    static constexpr int MROWS = MT * 16;
+    static constexpr bool kTensor = true;
+    // per-warp shared memory beyond the ring: the staged q rows (1 KiB granules)
+    static constexpr int kScratchBytes = kQSmem ? (MROWS * QSTRIDE + 1023) / 1024 * 1024 : 0;
+    static constexpr int kNbuf = 2;  // ring depth per warp (three CTAs of four warps fit an SM)
+
+    __device__ __forceinline__ void setup(uint8_t* scratch) {
+        qs_gen = scratch;
+        qs = smem_u32(scratch);
+    }
+
+    // stage q rows r < M of (b, hk) (16-bit storage) in this warp's scratch
+    __device__ __forceinline__ void stage_q_rows(const DecodeParams& p, int b, int hk, int lane) {
+        constexpr int VPR = D * 2 / 16;
+        const uint4* q = reinterpret_cast<const uint4*>(p.q);
+        for (int e = lane; e < MROWS * VPR; e += 32) {
+            const int r = e / VPR, v = e % VPR;
+            uint4 val = make_uint4(0u, 0u, 0u, 0u);
+            if (r < p.M) {
+                const int i = r / p.G, g = r % p.G;
+                val = __ldg(q + ((static_cast<long long>(b) * p.sq + i) * p.Hq + hk * p.G + g) * VPR + v);
+            }
+            *reinterpret_cast<uint4*>(qs_gen + r * QSTRIDE + v * 16) = val;
+        }
+        __syncwarp();
+    }
+
+    __device__ __forceinline__ void init(int) {}
+    __device__ __forceinline__ void load_q(const DecodeParams& p, int b, int hk, int lane) {
+        if constexpr (kQSmem)
+            stage_q_rows(p, b, hk, lane);
+        else
+            load_q_global(p, b, hk, lane);
+    }
+
+    // Q fragments straight from global memory: rows r < M of (b, hk), zero padding.
+    __device__ __forceinline__ void load_q_global(const DecodeParams& p, int b, int hk, int lane) {
+        static_assert(!kQSmem, "register Q fragments only for one row tile");
+        const int g = lane >> 2, tg = lane & 3;
+        const uint16_t* q = reinterpret_cast<const uint16_t*>(p.q);
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int r = mt * 16 + h * 8 + g;
+                const uint32_t* row = nullptr;
+                if (r < p.M) {
+                    const int i = r / p.G, gg = r % p.G;
+                    row = reinterpret_cast<const uint32_t*>(
+                        q + ((static_cast<long long>(b) * p.sq + i) * p.Hq + hk * p.G + gg) * D);
+                }
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    qa[mt][kk][h] = row ? __ldg(row + kk * 8 + tg) : 0u;
+                    qa[mt][kk][2 + h] = row ? __ldg(row + kk * 8 + 4 + tg) : 0u;
+                }
             }
     }
 
@@ -52,12 +135,25 @@ struct MmaWarp {
     // Fold one stage into the state.  Logits are scale2 * q.k + bias2 (log2
     // domain); key kt (0..15) is used by row `row` iff kt < nvalid and
     // visible(row, kt).  V rows at or past nvalid must be finite (zeroed).
-    template <class Visible>
+    // Row half h of row tile mt feeds P.V n-tile 2*mt + h; halves past NT
+    // hold only padding rows and are skipped.
+    static __device__ __forceinline__ constexpr bool half_used(int mt, int h) { return 2 * mt + h < NT; }
+
+    // Fold one stage into the state.  Logits are scale2 * q.k + bias2 (log2
+    // domain).  kMasked: key kt (0..15) is used by row `row` iff kt < nvalid
+    // and visible(row, kt), and V rows at or past nvalid must be finite
+    // (zeroed); otherwise all 16 keys are used by every row.
+    template <bool kMasked, class Visible>
     __device__ __forceinline__ void consume(uint32_t st, int half, int nvalid, float scale2, float bias2,
                                             Visible visible, int lane) {
-        const int g = lane >> 2, tg = lane & 3;
-        const int mi = lane >> 3, ri = lane & 7;
         float sacc[MT][2][4];
+        qk(st, sacc, lane);
+        softmax_pv<kMasked>(sacc, st + half, nvalid, scale2, bias2, visible, lane);
+    }
+
+    // S = Q K^T for the 16 keys of the K tile at `st`.
+    __device__ __forceinline__ void qk(uint32_t st, float (&sacc)[MT][2][4], int lane) const {
+        const int mi = lane >> 3, ri = lane & 7;
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -70,32 +166,47 @@ struct MmaWarp {
             ldsm_x4(st + swz((mi >> 1) * 8 + ri, (2 * kk + (mi & 1)) * 16), b00, b01, b10, b11);
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
-                mma16816<kBF16>(sacc[mt][0], qa[mt][kk], b00, b01);
-                mma16816<kBF16>(sacc[mt][1], qa[mt][kk], b10, b11);
+                uint32_t a[4];
+                q_frag(mt, kk, a, lane);
+                mma16816<kBF16>(sacc[mt][0], a, b00, b01);
+                mma16816<kBF16>(sacc[mt][1], a, b10, b11);
             }
         }
+    }
 
+    // Online softmax of S (scaled here), then O^T += V^T P^T with the V tile at `vt`.
+    template <bool kMasked, class Visible>
+    __device__ __forceinline__ void softmax_pv(float (&sacc)[MT][2][4], uint32_t vt, int nvalid, float scale2,
+                                               float bias2, Visible visible, int lane) {
+        const int g = lane >> 2, tg = lane & 3;
+        const int mi = lane >> 3, ri = lane & 7;
         float alpha[MT][2];
+        bool grew = false;
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
+                alpha[mt][h] = 1.f;
+                if (!half_used(mt, h)) continue;
                 const int row = mt * 16 + h * 8 + g;
                 float mx = -INFINITY;
 #pragma unroll
                 for (int n = 0; n < 2; ++n)
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        const int kt = n * 8 + 2 * tg + e;
-                        const bool ok = kt < nvalid && visible(row, kt);
-                        const float s = ok ? fmaf(sacc[mt][n][2 * h + e], scale2, bias2) : -INFINITY;
+                        float s = fmaf(sacc[mt][n][2 * h + e], scale2, bias2);
+                        if constexpr (kMasked) {
+                            const int kt = n * 8 + 2 * tg + e;
+                            if (!(kt < nvalid && visible(row, kt))) s = -INFINITY;
+                        }
                         sacc[mt][n][2 * h + e] = s;
                         mx = fmaxf(mx, s);
                     }
                 mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
                 mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
                 const float m_new = fmaxf(m_run[mt][h], mx);
-                const float m_use = m_new == -INFINITY ? 0.f : m_new;
+                const float m_use = (kMasked && m_new == -INFINITY) ? 0.f : m_new;
+                grew |= m_new > m_run[mt][h];
                 alpha[mt][h] = fast_exp2(m_run[mt][h] - m_use);
                 m_run[mt][h] = m_new;
                 float ls = 0.f;
@@ -113,29 +224,46 @@ struct MmaWarp {
                 l_run[mt][h] = l_run[mt][h] * alpha[mt][h] + ls;
             }
 
+        // rescale O^T columns (rows 8n + 2tg + e) only when some row's max moved
+        if (__any_sync(kFull, grew)) {
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                const int mt = n >> 1, h = n & 1;
+                const float a0 = __shfl_sync(kFull, alpha[mt][h], 4 * (2 * tg));
+                const float a1 = __shfl_sync(kFull, alpha[mt][h], 4 * (2 * tg + 1));
+#pragma unroll
+                for (int dt = 0; dt < D / 16; ++dt) {
+                    oacc[dt][n][0] *= a0;
+                    oacc[dt][n][1] *= a1;
+                    oacc[dt][n][2] *= a0;
+                    oacc[dt][n][3] *= a1;
+                }
+            }
+        }
         uint32_t pb[NT][2];
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
             const int mt = n >> 1, h = n & 1;
-            const float a0 = __shfl_sync(kFull, alpha[mt][h], 4 * (2 * tg));
-            const float a1 = __shfl_sync(kFull, alpha[mt][h], 4 * (2 * tg + 1));
-#pragma unroll
-            for (int dt = 0; dt < D / 16; ++dt) {
-                oacc[dt][n][0] *= a0;
-                oacc[dt][n][1] *= a1;
-                oacc[dt][n][2] *= a0;
-                oacc[dt][n][3] *= a1;
-            }
             pb[n][0] = pack2<kBF16>(sacc[mt][0][2 * h], sacc[mt][0][2 * h + 1]);
             pb[n][1] = pack2<kBF16>(sacc[mt][1][2 * h], sacc[mt][1][2 * h + 1]);
         }
 #pragma unroll
         for (int dt = 0; dt < D / 16; ++dt) {
             uint32_t va[4];
-            ldsm_x4_t(st + half + swz((mi >> 1) * 8 + ri, (2 * dt + (mi & 1)) * 16), va[0], va[1], va[2], va[3]);
+            ldsm_x4_t(vt + swz((mi >> 1) * 8 + ri, (2 * dt + (mi & 1)) * 16), va[0], va[1], va[2], va[3]);
 #pragma unroll
             for (int n = 0; n < NT; ++n) mma16816<kBF16>(oacc[dt][n], va, pb[n][0], pb[n][1]);
         }
+    }
+
+    // Full or masked stage, chosen per call (the choice is warp-uniform).
+    template <class Visible>
+    __device__ __forceinline__ void consume(uint32_t st, int half, int nvalid, bool masked, float scale2,
+                                            float bias2, Visible visible, int lane) {
+        if (masked)
+            consume<true>(st, half, nvalid, scale2, bias2, visible, lane);
+        else
+            consume<false>(st, half, nvalid, scale2, bias2, visible, lane);
     }
 
     // Sum each row's l over the four lanes that share it.
@@ -147,6 +275,39 @@ struct MmaWarp {
                 l_run[mt][h] += __shfl_xor_sync(kFull, l_run[mt][h], 1);
                 l_run[mt][h] += __shfl_xor_sync(kFull, l_run[mt][h], 2);
             }
+    }
+
+    __device__ __forceinline__ void finish() { reduce_l(); }
+
+    // After finish(): f(row, d, o / l) for every element this lane holds.
+    template <class F>
+    __device__ __forceinline__ void emit(F&& f, int lane) const {
+        const int g = lane >> 2, tg = lane & 3;
+        float lcol[NT][2];
+        column_rows_stat(l_run, lcol, lane);
+#pragma unroll
+        for (int dt = 0; dt < D / 16; ++dt)
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const float l = lcol[n][c & 1];
+                    f(n * 8 + 2 * tg + (c & 1), dt * 16 + g + (c >> 1) * 8, l > 0.f ? oacc[dt][n][c] / l : 0.f);
+                }
+    }
+
+    // After finish(): f(row, lse in log2 units, or -inf) once per row.
+    template <class F>
+    __device__ __forceinline__ void emit_lse(F&& f, int lane) const {
+        const int g = lane >> 2, tg = lane & 3;
+        if (tg == 0)
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const float l = l_run[mt][h];
+                    f(mt * 16 + h * 8 + g, l > 0.f ? m_run[mt][h] + __log2f(l) : -INFINITY);
+                }
     }
 
     // Row stats of the accumulator columns this lane holds: rows 8n + 2tg + e.

@@ -19,6 +19,7 @@ namespace pkd {
 
 constexpr int kSegNbuf = 2;
 constexpr int kMaxGroups = 64;
+constexpr int kMaxSegStages = 512;  // paged segments: page index of every stage of a CTA
 
 template <int D, int NT>
 struct SegShape {
@@ -33,8 +34,9 @@ struct SegShape {
     static constexpr int OFF_BARS = BIG;
     static constexpr int OFF_Q = OFF_BARS + kNW * kSegNbuf * 8;
     static constexpr int OFF_ML = OFF_Q + MROWS * QSTRIDE;
-    static constexpr int OFF_SEG = OFF_ML + 2 * kNW * MROWS * 4;        // used[g], prefix[g], bias2[g]
-    static constexpr int SMEM = OFF_SEG + 3 * (kMaxGroups + 1) * 4 + 1024;
+    static constexpr int OFF_SEG = OFF_ML + 2 * kNW * MROWS * 4;  // used, prefix, bias2, start, aligned start
+    static constexpr int OFF_PAGE = OFF_SEG + 5 * (kMaxGroups + 1) * 4;
+    static constexpr int SMEM = OFF_PAGE + kMaxSegStages * 4 + 1024;
 };
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -49,7 +51,7 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-template <int D, bool kBF16, int NT, bool kSegOut>
+template <int D, bool kBF16, int NT, bool kSegOut, bool kPaged>
 __global__ void __launch_bounds__(kNW * 32)
 segmented_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                  const SegmentParams p) {
@@ -63,6 +65,9 @@ segmented_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     int* su = reinterpret_cast<int*>(smem + S::OFF_SEG);    // used, clamped
     int* pre = su + (kMaxGroups + 1);                       // stage prefix (fused mode)
     float* sb = reinterpret_cast<float*>(pre + (kMaxGroups + 1));  // prior, log2 domain
+    int* ss = reinterpret_cast<int*>(sb + (kMaxGroups + 1));       // paged: first key of the segment
+    int* sa = ss + (kMaxGroups + 1);                               // paged: first key of its first stage
+    int* spage = reinterpret_cast<int*>(smem + S::OFF_PAGE);       // paged: page of every stage
 
     const int i = blockIdx.x, hk = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -73,8 +78,18 @@ segmented_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     if (tid < groups) {
         const int cap = tid < p.topk ? p.bs : p.local;
         int u = p.used[static_cast<long long>(i) * groups + tid];
-        su[tid] = u < 0 ? 0 : (u > cap ? cap : u);
+        u = u < 0 ? 0 : (u > cap ? cap : u);
         sb[tid] = tid < p.topk ? p.bias[static_cast<long long>(i) * p.topk + tid] * kLog2e : 0.f;
+        if constexpr (kPaged) {
+            // keys [start, start + used) of request row i; stages start on 16-key boundaries
+            int st = p.seg_start[static_cast<long long>(i) * groups + tid];
+            st = st < 0 ? 0 : st;
+            if (st > p.max_kv_len) st = p.max_kv_len;
+            if (u > p.max_kv_len - st) u = p.max_kv_len - st;
+            ss[tid] = st;
+            sa[tid] = st / kStageTok * kStageTok;
+        }
+        su[tid] = u;
     }
     if (tid == 0) {
         for (int k = 0; k < kNW * kSegNbuf; ++k) mbar_init(smem_u32(bars + k), 1);
@@ -93,15 +108,31 @@ segmented_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         }
     }
     __syncthreads();
+    // stages of segment g (16 keys each; a paged segment may start mid-stage)
+    auto nstages = [&](int g) {
+        if (su[g] <= 0) return 0;
+        return kPaged ? (ss[g] + su[g] - sa[g] + kStageTok - 1) / kStageTok : (su[g] + kStageTok - 1) / kStageTok;
+    };
     if (tid == 0) {
         int acc = 0;
         for (int g = 0; g < groups; ++g) {
             pre[g] = acc;
-            acc += (su[g] + kStageTok - 1) / kStageTok;
+            acc += nstages(g);
         }
-        pre[groups] = acc;
+        pre[groups] = acc < kMaxSegStages || !kPaged ? acc : kMaxSegStages;
     }
     __syncthreads();
+    if constexpr (kPaged) {
+        // page of every stage, looked up once so that no TMA issue waits on the table
+        for (int s2 = tid; s2 < pre[groups]; s2 += blockDim.x) {
+            int g = 0;
+            while (g + 1 < groups && pre[g + 1] <= s2) ++g;
+            const int tok0 = sa[g] + (s2 - pre[g]) * kStageTok;
+            int pg = p.block_table[static_cast<long long>(i) * p.bt_stride + tok0 / p.P];
+            spage[s2] = (pg < 0 || pg >= p.num_pages) ? -1 : pg;
+        }
+        __syncthreads();
+    }
 
     // stage list of this warp: fused mode takes stages round-robin over the
     // union; segment-output mode takes whole segments g = warp, warp + 4, ...
@@ -115,7 +146,7 @@ segmented_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             g = warp;
             int rem = k;
             while (g < groups) {
-                const int ns = (su[g] + kStageTok - 1) / kStageTok;
+                const int ns = pre[g + 1] - pre[g];
                 if (rem < ns) break;
                 rem -= ns;
                 g += kNW;
@@ -128,7 +159,7 @@ segmented_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         const int total = pre[groups];
         my_n = total > warp ? (total - warp + kNW - 1) / kNW : 0;
     } else {
-        for (int g = warp; g < groups; g += kNW) my_n += (su[g] + kStageTok - 1) / kStageTok;
+        for (int g = warp; g < groups; g += kNW) my_n += pre[g + 1] - pre[g];
     }
 
     uint8_t* ring_gen = smem + warp * kSegNbuf * S::STAGE;
@@ -138,10 +169,22 @@ segmented_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     auto issue = [&](int k) {
         int g, sidx;
         stage_of(k, g, sidx);
-        const long long row = row_base + (g < p.topk ? static_cast<long long>(g) * p.bs : static_cast<long long>(p.topk) * p.bs) +
-                              static_cast<long long>(sidx) * kStageTok;
         const uint32_t buf = ring + (k % kSegNbuf) * S::STAGE;
         const uint32_t bar = bar0 + 8 * (k % kSegNbuf);
+        if constexpr (kPaged) {
+            const int pg = spage[pre[g] + sidx];
+            if (pg < 0) {
+                mbar_arrive(bar);
+                return;
+            }
+            const int tok0 = sa[g] + sidx * kStageTok;
+            const int crow = (pg * p.Hkv + hk) * p.P + tok0 % p.P;
+            mbar_arrive_expect_tx(bar, S::STAGE);
+            tma_load_3d(buf, &kmap, 0, crow, 0, bar, pol);
+            return;
+        }
+        const long long row = row_base + (g < p.topk ? static_cast<long long>(g) * p.bs : static_cast<long long>(p.topk) * p.bs) +
+                              static_cast<long long>(sidx) * kStageTok;
         mbar_arrive_expect_tx(bar, S::STAGE);
 #pragma unroll
         for (int bx = 0; bx < D * 2 / 128; ++bx) {
@@ -204,18 +247,27 @@ segmented_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         consumed = k + 1;
         int g, sidx;
         stage_of(k, g, sidx);
-        const int nvalid = min(kStageTok, su[g] - sidx * kStageTok);
+        // keys [lo, nvalid) of this stage belong to the segment
+        int nvalid, lo = 0;
+        if constexpr (kPaged) {
+            const int tok0 = sa[g] + sidx * kStageTok;
+            nvalid = min(kStageTok, ss[g] + su[g] - tok0);
+            lo = ss[g] - tok0;
+            if (spage[pre[g] + sidx] < 0) nvalid = 0;
+        } else {
+            nvalid = min(kStageTok, su[g] - sidx * kStageTok);
+        }
         const uint32_t st = ring + buf * S::STAGE;
         if (nvalid < kStageTok) zero_tail_v<D, 2>(ring_gen + buf * S::STAGE, nvalid, lane);
-        wp.consume(st, S::HALF, nvalid, p.scale_log2, kSegOut ? 0.f : sb[g],
-                   [&](int row, int) { return row < M; }, lane);
+        wp.consume(st, S::HALF, nvalid, nvalid < kStageTok || lo > 0, p.scale_log2, kSegOut ? 0.f : sb[g],
+                   [&](int row, int kt) { return row < M && kt >= lo; }, lane);
         __syncwarp();
         if (lane == 0 && k + kSegNbuf < my_n) {
             fence_proxy_async();
             issue(k + kSegNbuf);
         }
         if constexpr (kSegOut) {
-            if ((sidx + 1) * kStageTok >= su[g]) emit_segment(g);
+            if (sidx + 1 >= pre[g + 1] - pre[g]) emit_segment(g);
         }
     }
     if (timed_out) {
@@ -316,10 +368,10 @@ __global__ void __launch_bounds__(128) lse_merge_kernel(const MergeParams p) {
     if (lane == 0 && p.lse_out) p.lse_out[nn * p.heads + h] = total;
 }
 
-template <int D, bool kBF16, int NT, bool kSegOut>
-static cudaError_t launch_seg_one(const SegmentParams& p, cudaStream_t stream) {
+template <int D, bool kBF16, int NT, bool kSegOut, bool kPaged>
+static cudaError_t launch_seg_paged(const SegmentParams& p, cudaStream_t stream) {
     using S = SegShape<D, NT>;
-    auto kern = segmented_kernel<D, kBF16, NT, kSegOut>;
+    auto kern = segmented_kernel<D, kBF16, NT, kSegOut, kPaged>;
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
@@ -328,6 +380,12 @@ static cudaError_t launch_seg_one(const SegmentParams& p, cudaStream_t stream) {
     }
     kern<<<dim3(p.n, p.Hkv), kNW * 32, S::SMEM, stream>>>(p.kmap, p.vmap, p);
     return cudaGetLastError();
+}
+
+template <int D, bool kBF16, int NT, bool kSegOut>
+static cudaError_t launch_seg_one(const SegmentParams& p, cudaStream_t stream) {
+    return p.paged ? launch_seg_paged<D, kBF16, NT, kSegOut, true>(p, stream)
+                   : launch_seg_paged<D, kBF16, NT, kSegOut, false>(p, stream);
 }
 
 template <int D, bool kBF16, bool kSegOut>

@@ -7,7 +7,12 @@
 namespace pkd {
 
 struct SegmentParams {
-    CUtensorMap kmap, vmap;   // 3-D maps over k, v: {head_dim, Hkv, rows}
+    CUtensorMap kmap, vmap;   // 3-D maps over k, v: {head_dim, Hkv, rows}; paged: kmap is the
+                              // cache's stage map {128-byte chunk, pages*Hkv*P rows, chunks}
+    const int32_t* block_table;  // paged: [n, bt_stride]
+    const int32_t* seg_start;    // paged: [n, topk+1] first key position of each segment
+    long long bt_stride, num_pages;
+    int P, max_kv_len, paged;
     const void* q;            // [n, Hq, D]
     const int32_t* used;      // [n, topk+1]
     const float* bias;        // [n, topk]

@@ -45,16 +45,24 @@ def test_workspace_plan_is_a_host_function(lib):
     assert n > 0 and n % 256 == 0
     # more splits for longer capacity
     assert pkd.workspace_size(8, 1, 64, 8, 128, 64, 131072, pkd.FP8_E4M3) > 0
-    # explicit chunk: 4096 / 256 = 16 splits -> partials [512 units, 16, 4 rows, 128] fp32 at least
-    m = pkd.workspace_size(64, 1, 32, 8, 128, 16, 4096, pkd.BF16, chunk_tokens=256)
+    # chunked grid, explicit chunk: 4096 / 256 = 16 splits -> partials [512 units, 16, 4 rows, 128] fp32
+    m = pkd.workspace_size(64, 1, 32, 8, 128, 16, 4096, pkd.BF16, chunk_tokens=256, flags=pkd.FLAG_GRID)
     assert m >= 512 * 16 * 4 * 128 * 4
+    # flat partition: two partial slots per worker warp, independent of the lengths
+    f1 = pkd.workspace_size(64, 1, 32, 8, 128, 16, 4096, pkd.BF16)
+    f2 = pkd.workspace_size(64, 1, 32, 8, 128, 16, 131072, pkd.BF16)
+    assert f1 == f2 and f1 >= 2048 * 2 * 4 * 128 * 4
+    # batches above the flat kernel's table size use the chunked grid
+    assert pkd.workspace_size(2048, 1, 32, 8, 128, 16, 4096, pkd.BF16) == \
+        pkd.workspace_size(2048, 1, 32, 8, 128, 16, 4096, pkd.BF16, flags=pkd.FLAG_GRID)
 
 
 @pytest.mark.parametrize("args,needle", [
     ((2, 1, 6, 4, 128, 16, 100, pkd.BF16), "multiple of num_kv_heads"),
     ((2, 1, 8, 2, 96, 16, 100, pkd.BF16), "head_dim"),
     ((2, 1, 8, 2, 128, 8, 100, pkd.BF16), "page_size"),
-    ((2, 4, 32, 8, 128, 16, 100, pkd.FP8_E4M3), "fp8"),
+    ((2, 4, 32, 8, 128, 16, 100, pkd.FP8_E4M3, 0, 0, pkd.FLAG_FMA), "fp8"),
+    ((2, 4, 32, 8, 128, 16, 100, pkd.FP8_E4M3, 0, 0, pkd.FLAG_GRID), "fp8"),
     ((2, 16, 32, 8, 128, 16, 100, pkd.BF16), "> 32"),
     ((2, 1, 8, 2, 64, 16, 100, pkd.FP8_E4M3), "head_dim 128"),
 ])

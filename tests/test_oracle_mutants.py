@@ -37,6 +37,16 @@ MUTANTS = {
     "bf16 decoded as low half": ("uint32_t u = ((uint32_t)h) << 16;", "uint32_t u = ((uint32_t)h) << 15;"),
     "e4m3 exponent bias 8": ("v = ldexp((double)(8 + m), e - 10);", "v = ldexp((double)(8 + m), e - 11);"),
     "causal position off by one": ("long pos = L - sq + i;", "long pos = L - sq + i - 1;"),
+    "e4m3 mantissa truncated": ("double t = nearbyint((ldexp(a, -e) - 1.0) * 8.0);",
+                                "double t = floor((ldexp(a, -e) - 1.0) * 8.0);"),
+    "e4m3 overflow to the NaN code": ("if (a >= 448.0) return sign | 0x7E;", "if (a >= 448.0) return sign | 0x7F;"),
+    "cache write V over K": ("((uint16_t*)cache)[dst + D + d] = ((const uint16_t*)value)[src + d];",
+                             "((uint16_t*)cache)[dst + d] = ((const uint16_t*)value)[src + d];"),
+    "cache write slot offset": ("const long page = (long)(s / P), off = (long)(s % P);",
+                                "const long page = (long)(s / P), off = (long)((s + 1) % P);"),
+    "cache write key scale ignored": ("orc_encode_e4m3(kx / k_scale);", "orc_encode_e4m3(kx);"),
+    "paged segment key off by one": ("const long j = st + t;\n                    const long page = block_table[(long)i * bt_stride + j / P];\n                    const size_t kbase",
+                                     "const long j = st + t + 1;\n                    const long page = block_table[(long)i * bt_stride + j / P];\n                    const size_t kbase"),
 }
 
 PINS = [
@@ -55,6 +65,13 @@ PINS = [
     pins.test_lse_merge_dead_parts_and_all_dead,
     lambda: pins.test_paged_decode_matches_brute_force(dict(sq=3, causal=True, window=10)),
     lambda: pins.test_paged_decode_matches_brute_force(dict(sq=3, window=20)),
+    pins.test_encode_e4m3_exact_values_round_trip,
+    pins.test_encode_e4m3_matches_torch_round_to_nearest_even,
+    pins.test_encode_e4m3_saturates,
+    pins.test_cache_write_16bit_places_rows_by_slot,
+    pins.test_cache_write_fp8_quantises_each_element,
+    pins.test_paged_segments_equal_contiguous_segments_after_gathering,
+    pins.test_paged_segments_single_segment_is_window_decode,
 ]
 
 

@@ -365,3 +365,136 @@ def test_lse_merge_dead_parts_and_all_dead():
     # closed form for row 2: weights softmax(lse)
     w = np.exp(pl[2] - np.log(np.exp(pl[2]).sum(0)))
     assert np.allclose(out[2], np.einsum("sh,shd->hd", w, po[2]), atol=1e-13)
+
+
+# ----------------------------------------------------------- cache write
+def _all_finite_e4m3():
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    return codes, torch.from_numpy(codes).view(torch.float8_e4m3fn).float().numpy()
+
+
+def test_encode_e4m3_exact_values_round_trip():
+    codes, vals = _all_finite_e4m3()
+    got = oracle.encode_e4m3(vals)
+    # -0.0 and +0.0 keep their sign; every finite code maps back to itself
+    assert np.array_equal(got, codes)
+
+
+def test_encode_e4m3_matches_torch_round_to_nearest_even():
+    rng = np.random.default_rng(12)
+    mags = np.exp(rng.uniform(np.log(2.0 ** -12), np.log(440.0), 200_000)).astype(np.float32)
+    x = mags * rng.choice([-1.0, 1.0], mags.size).astype(np.float32)
+    # ties: midpoints between neighbouring finite codes (round half to even decides)
+    _, vals = _all_finite_e4m3()
+    pos = np.unique(vals[vals >= 0])
+    mids = ((pos[:-1].astype(np.float64) + pos[1:]) / 2).astype(np.float32)
+    x = np.concatenate([x, mids, -mids])
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.encode_e4m3(x), ref)
+
+
+def test_encode_e4m3_saturates():
+    got = oracle.encode_e4m3(np.array([448.0, 463.9, 464.0, 1e6, np.inf, -500.0, -np.inf], np.float32))
+    assert got.tolist() == [0x7E, 0x7E, 0x7E, 0x7E, 0x7E, 0xFE, 0xFE]
+
+
+def _cache_write_case(dtype_in="bf16", kv="bf16", T=37, Hkv=2, D=16, P=16, num_pages=9, seed=4):
+    rng = np.random.default_rng(seed)
+    key = wl.normal_storage(rng, (T, Hkv, D), dtype_in)
+    value = wl.normal_storage(rng, (T, Hkv, D), dtype_in)
+    slots = rng.permutation(num_pages * P)[:T].astype(np.int64)
+    slots[[3, 11]] = -1                                   # padding tokens
+    cache = wl.normal_storage(rng, (num_pages, Hkv, P, 2 * D), kv)
+    return key, value, slots, cache
+
+
+def test_cache_write_16bit_places_rows_by_slot():
+    key, value, slots, cache = _cache_write_case()
+    out = oracle.cache_write(key, value, "bf16", slots, cache, "bf16", num_kv_heads=2, head_dim=16, page_size=16)
+    expect = cache.copy()
+    for t, s in enumerate(slots):
+        if s < 0:
+            continue
+        expect[s // 16, :, s % 16, :16] = key[t]
+        expect[s // 16, :, s % 16, 16:] = value[t]
+    assert np.array_equal(out, expect)
+
+
+def test_cache_write_fp8_quantises_each_element():
+    key, value, slots, cache = _cache_write_case(kv="fp8")
+    ks, vs = 1.0 / 64, 1.0 / 32
+    out = oracle.cache_write(key, value, "bf16", slots, cache, "fp8", num_kv_heads=2, head_dim=16, page_size=16,
+                             k_scale=ks, v_scale=vs)
+    kf = brute.decode(key, "bf16").astype(np.float32)
+    vf = brute.decode(value, "bf16").astype(np.float32)
+    kq = torch.from_numpy(np.clip(kf / np.float32(ks), -448, 448)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    vq = torch.from_numpy(np.clip(vf / np.float32(vs), -448, 448)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    expect = cache.copy()
+    for t, s in enumerate(slots):
+        if s >= 0:
+            expect[s // 16, :, s % 16, :16] = kq[t]
+            expect[s // 16, :, s % 16, 16:] = vq[t]
+    assert np.array_equal(out, expect)
+
+
+def test_cache_write_then_decode_reads_what_was_written():
+    """A cache filled through cache_write decodes the same as one laid out directly."""
+    P, D, Hkv = 16, 16, 2
+    c = _small_case(seq_lens=[40, 17], num_heads=4, num_kv_heads=Hkv, head_dim=D, page_size=P)
+    keys = {}
+    blank = np.zeros_like(c.kv_cache)
+    blank[c.poison_page] = c.kv_cache[c.poison_page]
+    written = blank
+    for b in range(c.batch):
+        L = int(c.seq_lens[b])
+        toks = np.arange(L)
+        slots = (c.block_table[b, toks // P].astype(np.int64) * P + toks % P)
+        k = np.stack([c.kv_cache[c.block_table[b, t // P], :, t % P, :D] for t in toks])
+        v = np.stack([c.kv_cache[c.block_table[b, t // P], :, t % P, D:] for t in toks])
+        written = oracle.cache_write(k, v, "bf16", slots, written, "bf16", num_kv_heads=Hkv, head_dim=D, page_size=P)
+    o1, l1 = _run(c)
+    o2, l2 = oracle.paged_decode(c.q, c.dtype, written, c.dtype, c.block_table, c.seq_lens, **c.oracle_kwargs())
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+# ------------------------------------------------------ paged segments
+def test_paged_segments_equal_contiguous_segments_after_gathering():
+    """Gathering each segment's keys into contiguous rows (by a plain loop over
+    the block table) and running the contiguous-segment oracle gives the same."""
+    s = wl.paged_segment_case(n=5, num_heads=4, num_kv_heads=2, head_dim=16, page_size=16, topk=3, bs=24,
+                              local=32, seed=9, seq_range=(40, 200))
+    out, so, sl = oracle.segmented_paged(s.q, s.dtype, s.kv_cache, s.block_table, s.seg_start, s.used, s.bias,
+                                         num_kv_heads=2, page_size=16, topk=3, bs=24, local=32,
+                                         return_segments=True)
+    rows = 3 * 24 + 32
+    k = np.zeros((5 * rows, 2, 16), np.uint16)
+    v = np.zeros_like(k)
+    for i in range(5):
+        for g in range(4):
+            off = i * rows + (g * 24 if g < 3 else 72)
+            for t in range(int(s.used[i, g])):
+                j = int(s.seg_start[i, g]) + t
+                page = s.block_table[i, j // 16]
+                k[off + t] = s.kv_cache[page, :, j % 16, :16]
+                v[off + t] = s.kv_cache[page, :, j % 16, 16:]
+    ref, rso, rsl = oracle.segmented_attention(s.q, k, v, s.dtype, s.used, s.bias, topk=3, bs=24, local=32,
+                                               num_kv_heads=2, return_segments=True)
+    assert np.array_equal(out, ref) and np.array_equal(so, rso) and np.array_equal(sl, rsl)
+
+
+def test_paged_segments_single_segment_is_window_decode():
+    """One local segment covering the last w keys equals paged decode of that
+    key range (a table sliced to start there, with the length renumbered)."""
+    c = _small_case(seq_lens=[64, 96], num_heads=4, num_kv_heads=2)
+    w = 32
+    seg_start = (c.seq_lens - w).reshape(2, 1).astype(np.int32)
+    used = np.full((2, 1), w, np.int32)
+    q3 = np.ascontiguousarray(c.q[:, 0])
+    out = oracle.segmented_paged(q3, c.dtype, c.kv_cache, c.block_table, seg_start, used, np.zeros((2, 0)),
+                                 num_kv_heads=2, page_size=16, topk=0, bs=0, local=w)
+    for b in range(2):
+        start = int(c.seq_lens[b]) - w       # a page boundary here
+        table = np.ascontiguousarray(c.block_table[b:b + 1, start // 16:])
+        o, _ = oracle.paged_decode(c.q[b:b + 1], c.dtype, c.kv_cache, c.dtype, table, np.array([w], np.int32),
+                                   **dict(c.oracle_kwargs(), scale=16 ** -0.5))
+        assert np.allclose(out[b], o[0, 0], atol=1e-13, rtol=0)

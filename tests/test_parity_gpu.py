@@ -4,6 +4,8 @@ Small cases span several 16-key stages, several Split-KV chunks and ragged
 tails; full-size workloads are compared on all (or sampled) requests.  The
 probes check the page gather bit-exactly.
 """
+import zlib
+
 import numpy as np
 import pytest
 import torch
@@ -38,47 +40,59 @@ LENS = [1, 15, 16, 17, 200, 1000, 777, 64, 0, 333]
 
 SMALL = {
     # name: paged_case kwargs, call kwargs
-    "bf16_g4_fma": (dict(seq_lens=LENS), dict()),
-    "bf16_g4_mma": (dict(seq_lens=LENS), dict(mma_small_m=True)),
-    "bf16_g4_fma_chunk16": (dict(seq_lens=LENS), dict(chunk_tokens=16)),
-    "bf16_g4_mma_chunk32": (dict(seq_lens=LENS), dict(chunk_tokens=32, mma_small_m=True)),
-    "fp16_g4_fma": (dict(seq_lens=LENS, dtype="fp16"), dict(chunk_tokens=64)),
-    "fp16_g4_mma": (dict(seq_lens=LENS, dtype="fp16"), dict(mma_small_m=True, chunk_tokens=128)),
+    "bf16_g4": (dict(seq_lens=LENS), dict()),
+    "bf16_g4_chunk16": (dict(seq_lens=LENS), dict(chunk_tokens=16)),
+    "bf16_g4_chunk32": (dict(seq_lens=LENS), dict(chunk_tokens=32)),
+    "fp16_g4": (dict(seq_lens=LENS, dtype="fp16"), dict(chunk_tokens=64)),
+    "fp16_g4_chunk128": (dict(seq_lens=LENS, dtype="fp16"), dict(chunk_tokens=128)),
     "bf16_d64_p32": (dict(seq_lens=LENS, head_dim=64, page_size=32), dict(chunk_tokens=64)),
-    "bf16_d64_p32_mma": (dict(seq_lens=LENS, head_dim=64, page_size=32), dict(mma_small_m=True)),
+    "bf16_d64_p32_auto": (dict(seq_lens=LENS, head_dim=64, page_size=32), dict()),
     "bf16_mha_g1": (dict(seq_lens=LENS, num_heads=8, num_kv_heads=8), dict(chunk_tokens=48)),
     "bf16_g2_sq1": (dict(seq_lens=LENS, num_heads=4, num_kv_heads=2), dict()),
-    "bf16_g8_fma": (dict(seq_lens=LENS, num_heads=64, num_kv_heads=8), dict(chunk_tokens=96)),
-    "bf16_g8_mma": (dict(seq_lens=LENS, num_heads=64, num_kv_heads=8), dict(mma_small_m=True)),
+    "bf16_g8": (dict(seq_lens=LENS, num_heads=64, num_kv_heads=8), dict(chunk_tokens=96)),
+    "bf16_g8_auto": (dict(seq_lens=LENS, num_heads=64, num_kv_heads=8), dict()),
     "bf16_sq3_g4_m12": (dict(seq_lens=LENS, sq=3), dict(chunk_tokens=64)),
     "bf16_sq8_g4_m32": (dict(seq_lens=LENS, sq=8), dict(chunk_tokens=128)),
     "bf16_sq8_g4_m32_auto": (dict(seq_lens=LENS, sq=8), dict()),
     "bf16_sq5_g4_m20": (dict(seq_lens=LENS, sq=5, head_dim=64), dict(chunk_tokens=64)),
     "bf16_sq8_window100": (dict(seq_lens=LENS, sq=8, window=100), dict(chunk_tokens=32)),
-    "bf16_sq1_window40_fma": (dict(seq_lens=LENS, window=40), dict()),
+    "bf16_sq1_window40": (dict(seq_lens=LENS, window=40), dict()),
     "bf16_p64_window300": (dict(seq_lens=LENS, page_size=64, window=300), dict(chunk_tokens=128)),
     "bf16_causal_sq4_m16": (dict(seq_lens=LENS, sq=4, causal=True), dict(chunk_tokens=64)),
     "bf16_causal_sq4_window50": (dict(seq_lens=LENS, sq=4, causal=True, window=50), dict(chunk_tokens=32)),
-    "bf16_causal_sq2_g2_fma": (dict(seq_lens=LENS, sq=2, num_heads=4, num_kv_heads=2, causal=True, window=30),
-                               dict()),
+    "bf16_causal_sq2_g2": (dict(seq_lens=LENS, sq=2, num_heads=4, num_kv_heads=2, causal=True, window=30), dict()),
     "fp8_g8": (dict(seq_lens=LENS, dtype="fp8", num_heads=64, num_kv_heads=8), dict(chunk_tokens=64)),
     "fp8_g4_p64": (dict(seq_lens=LENS, dtype="fp8", page_size=64), dict()),
     "fp8_g2_window": (dict(seq_lens=LENS, dtype="fp8", num_heads=16, num_kv_heads=8, window=100), dict()),
+    "fp8_sq4_g4_m16": (dict(seq_lens=LENS, dtype="fp8", sq=4), dict()),
+    "fp8_sq8_g4_m32_causal": (dict(seq_lens=LENS, dtype="fp8", sq=8, causal=True, window=200), dict()),
 }
 
+# kernel variants: persistent flat partition / one CTA per chunk; tensor / CUDA cores
+VARIANTS = {"flat": dict(), "grid": dict(grid=True), "flat_fma": dict(force_fma=True),
+            "grid_fma": dict(grid=True, force_fma=True)}
 
+
+def _m(ckw):
+    return ckw.get("sq", 1) * ckw.get("num_heads", 32) // ckw.get("num_kv_heads", 8)
+
+
+@pytest.mark.parametrize("variant", sorted(VARIANTS))
 @pytest.mark.parametrize("name", sorted(SMALL))
-def test_small_cases_match_oracle(name):
+def test_small_cases_match_oracle(name, variant):
     ckw, kw = SMALL[name]
-    case = wl.paged_case(name=name, seed=hash(name) % 1000, **ckw)
-    _check(case, **kw)
+    vkw = VARIANTS[variant]
+    if (vkw.get("force_fma") or (vkw.get("grid") and ckw.get("dtype") == "fp8")) and _m(ckw) > 8:
+        pytest.skip("the CUDA-core kernel takes M <= 8 (fp8 in the chunked grid always runs on it)")
+    case = wl.paged_case(name=name, seed=zlib.crc32(name.encode()) % 1000, **ckw)
+    _check(case, **kw, **vkw)
 
 
-def test_tiny_workload_both_paths():
+def test_tiny_workload_all_variants():
     case = wl.tiny_decode()
-    _check(case)
-    _check(case, mma_small_m=True)
-    _check(case, chunk_tokens=16)
+    for vkw in VARIANTS.values():
+        _check(case, **vkw)
+    _check(case, chunk_tokens=16, grid=True)
 
 
 def test_results_are_deterministic():
@@ -88,8 +102,8 @@ def test_results_are_deterministic():
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
-@pytest.mark.parametrize("mma", [False, True])
-def test_argmax_probe_gathers_bit_exactly(mma):
+@pytest.mark.parametrize("variant", sorted(VARIANTS))
+def test_argmax_probe_gathers_bit_exactly(variant):
     """q equal to one visible key and a huge scale: every other weight underflows
     to 0 and the output must be that key's V row, bit for bit."""
     case = wl.paged_case(name="probe", seq_lens=[37, 300, 129], num_heads=8, num_kv_heads=2, window=64,
@@ -107,21 +121,21 @@ def test_argmax_probe_gathers_bit_exactly(mma):
             case.q[b, 0, h] = case.kv_cache[page, h // 4, t % P, :D]
             targets[(b, h)] = (page, h // 4, t % P)
     case.scale = 100.0
-    out, _ = gu.run_paged(case, mma_small_m=mma, chunk_tokens=32)
+    out, _ = gu.run_paged(case, chunk_tokens=32, **VARIANTS[variant])
     got_bits = torch.from_numpy(out).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     for (b, h), (page, hk, slot) in targets.items():
         assert np.array_equal(got_bits[b, 0, h], case.kv_cache[page, hk, slot, D:]), (b, h)
 
 
-@pytest.mark.parametrize("mma", [False, True])
-def test_constant_v_is_exact_and_nan_pages_are_never_read(mma):
+@pytest.mark.parametrize("variant", sorted(VARIANTS))
+def test_constant_v_is_exact_and_nan_pages_are_never_read(variant):
     case = wl.paged_case(name="constv", seq_lens=[37, 300, 1, 129, 700], seed=5)
     one = 0x3F80
     P, D = case.page_size, case.head_dim
     for b in range(case.batch):
         for j in range(int(case.seq_lens[b])):
             case.kv_cache[case.block_table[b, j // P], :, j % P, D:] = one
-    out, lse = gu.run_paged(case, mma_small_m=mma, chunk_tokens=64)
+    out, lse = gu.run_paged(case, chunk_tokens=64, **VARIANTS[variant])
     assert np.all(out == 1.0)
     assert np.all(np.isfinite(lse))
 
@@ -201,9 +215,10 @@ def test_gqa_decode_b64_full():
     _check(case)
 
 
-def test_gqa_decode_b64_tensor_core_variant():
+@pytest.mark.parametrize("variant", ["grid", "flat_fma"])
+def test_gqa_decode_b64_other_variants(variant):
     case = wl.gqa_decode_b64()
-    _check(case, mma_small_m=True)
+    _check(case, **VARIANTS[variant])
 
 
 @pytest.mark.parametrize("window", [0, 4096])
@@ -212,6 +227,7 @@ def test_query_block_sq8_sampled(window):
     _check(case, batch_index=[0, 5, 11, 17, 23, 31])
 
 
-def test_fp8_long_b8_sampled():
+@pytest.mark.parametrize("variant", ["flat", "flat_fma"])
+def test_fp8_long_b8_sampled(variant):
     case = wl.fp8_long_b8()
-    _check(case, batch_index=[0, 7])
+    _check(case, batch_index=[0, 7], **VARIANTS[variant])

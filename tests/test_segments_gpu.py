@@ -1,4 +1,6 @@
 """GPU parity of DASH segmented attention (+ combine) and of the LSE merge."""
+import zlib
+
 import numpy as np
 import pytest
 import torch
@@ -56,13 +58,13 @@ SMALL = {
 
 @pytest.mark.parametrize("name", sorted(SMALL))
 def test_small_segments_fused(name):
-    s = wl.segment_case(name=name, seed=hash(name) % 997, **SMALL[name])
+    s = wl.segment_case(name=name, seed=zlib.crc32(name.encode()) % 997, **SMALL[name])
     gu.assert_close(_run(s), _oracle(s), gu.TOL_OUT, name)
 
 
 @pytest.mark.parametrize("name", sorted(SMALL))
 def test_small_segments_with_per_segment_results(name):
-    s = wl.segment_case(name=name, seed=hash(name) % 991, **SMALL[name])
+    s = wl.segment_case(name=name, seed=zlib.crc32(name.encode()) % 991, **SMALL[name])
     out, so, sl = _run(s, segments=True)
     ro, rso, rsl = _oracle(s, segments=True)
     gu.assert_close(out, ro, gu.TOL_OUT, name + " out")
@@ -117,3 +119,50 @@ def test_lse_merge_matches_oracle(with_prior, with_live):
                               None if prior is None else prior.astype(np.float64), live)
     gu.assert_close(out.double().cpu().numpy(), ro, 1e-5, "merge out")
     gu.assert_close(lse.double().cpu().numpy(), rl, 1e-5, "merge lse")
+
+
+# ------------------------------------------------ segments from the paged cache
+def _run_paged(s, segments=False):
+    import paged_kv_decode_15_gb300 as pkd
+    bias = gu.to_dev(s.bias, "fp32") if s.topk else torch.zeros((s.n, 0), dtype=torch.float32, device="cuda")
+    r = pkd.segmented_attention_paged(gu.to_dev(s.q, s.dtype), gu.to_dev(s.kv_cache, s.dtype),
+                                      gu.to_dev(s.block_table, "int32"), gu.to_dev(s.seg_start, "int32"),
+                                      gu.to_dev(s.used, "int32"), bias, s.bs, s.local, return_segments=segments)
+    torch.cuda.synchronize()
+    if segments:
+        return tuple(t.double().cpu().numpy() for t in r)
+    return r.double().cpu().numpy()
+
+
+def _oracle_paged(s, segments=False):
+    return oracle.segmented_paged(s.q, s.dtype, s.kv_cache, s.block_table, s.seg_start, s.used, s.bias,
+                                  num_kv_heads=s.num_kv_heads, page_size=s.page_size, topk=s.topk, bs=s.bs,
+                                  local=s.local, return_segments=segments, threads=gu.THREADS)
+
+
+PAGED = {
+    "g4_topk3_bs24": dict(n=7, num_heads=8, num_kv_heads=2, topk=3, bs=24, local=40, seq_range=(60, 400)),
+    "g8_d64_p32": dict(n=6, num_heads=16, num_kv_heads=2, head_dim=64, page_size=32, topk=4, bs=16, local=48,
+                       seq_range=(100, 300)),
+    "fp16_mha": dict(n=5, num_heads=4, num_kv_heads=4, topk=2, bs=64, local=16, dtype="fp16",
+                     seq_range=(200, 600)),
+    "local_only": dict(n=4, num_heads=8, num_kv_heads=2, topk=0, bs=16, local=72, seq_range=(80, 200)),
+    "many_empty": dict(n=9, num_heads=8, num_kv_heads=2, topk=6, bs=32, local=24, p_empty=0.7,
+                       seq_range=(100, 500)),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PAGED))
+def test_paged_segments_match_oracle(name):
+    s = wl.paged_segment_case(name=name, seed=zlib.crc32(name.encode()) % 983, **PAGED[name])
+    gu.assert_close(_run_paged(s), _oracle_paged(s), gu.TOL_OUT, name)
+    out, so, sl = _run_paged(s, segments=True)
+    ro, rso, rsl = _oracle_paged(s, segments=True)
+    gu.assert_close(out, ro, gu.TOL_OUT, name + " out")
+    gu.assert_close(so, rso, gu.TOL_OUT, name + " seg_out")
+    gu.assert_close(sl, rsl, gu.TOL_LSE, name + " seg_lse")
+
+
+def test_dash_paged_n256_full():
+    s = wl.dash_paged_n256()
+    gu.assert_close(_run_paged(s), _oracle_paged(s), gu.TOL_OUT, "dash paged")

@@ -262,8 +262,113 @@ def segment_case(*, name="segments", n=256, num_heads=32, num_kv_heads=8, head_d
                        num_kv_heads=num_kv_heads, topk=topk, bs=bs, local=local)
 
 
+@dataclasses.dataclass
+class PagedSegmentCase:
+    """DASH segments as key ranges of each query's request in a paged cache."""
+    name: str
+    q: np.ndarray            # [n, Hq, D] storage
+    kv_cache: np.ndarray     # [num_pages, Hkv, P, 2D] storage
+    block_table: np.ndarray  # int32 [n, W]
+    seq_lens: np.ndarray     # int32 [n]
+    seg_start: np.ndarray    # int32 [n, topk+1]
+    used: np.ndarray         # int32 [n, topk+1]
+    bias: np.ndarray         # float32 [n, topk]
+    dtype: str
+    num_kv_heads: int
+    page_size: int
+    topk: int
+    bs: int
+    local: int
+
+    @property
+    def n(self):
+        return int(self.q.shape[0])
+
+
+def paged_segment_case(*, name="paged_segments", n=16, seq_lens=None, num_heads=32, num_kv_heads=8, head_dim=128,
+                       page_size=16, topk=8, bs=64, local=128, dtype="bf16", seed=0, p_empty=0.1,
+                       seq_range=(1024, 4096)) -> PagedSegmentCase:
+    """Each query is one request: its gathered segments are topk distinct
+    bs-aligned blocks of its history (a random used prefix, 0 with p_empty),
+    and its local segment is the last `used` keys (used ~ U[1, local])."""
+    rng = np.random.default_rng(seed)
+    lens = (np.asarray(seq_lens, np.int32) if seq_lens is not None
+            else rng.integers(seq_range[0], seq_range[1] + 1, size=n).astype(np.int32))
+    base = paged_case(name=name, seq_lens=lens, sq=1, num_heads=num_heads, num_kv_heads=num_kv_heads,
+                      head_dim=head_dim, page_size=page_size, dtype=dtype, seed=seed + 1)
+    groups = topk + 1
+    seg_start = np.zeros((n, groups), np.int32)
+    used = np.zeros((n, groups), np.int32)
+    for i in range(n):
+        L = int(lens[i])
+        u_loc = int(rng.integers(1, min(local, L) + 1))
+        seg_start[i, topk] = L - u_loc
+        used[i, topk] = u_loc
+        nblocks = max(1, (L - u_loc) // bs)
+        blocks = rng.choice(nblocks, size=topk, replace=nblocks < topk)
+        for g in range(topk):
+            seg_start[i, g] = int(blocks[g]) * bs
+            room = max(0, min(bs, L - seg_start[i, g]))
+            used[i, g] = 0 if (rng.random() < p_empty or room == 0) else int(rng.integers(1, room + 1))
+    bias = rng.standard_normal((n, topk), dtype=np.float32)
+    q = normal_storage(rng, (n, num_heads, head_dim), dtype)
+    return PagedSegmentCase(name=name, q=q, kv_cache=base.kv_cache, block_table=base.block_table, seq_lens=lens,
+                            seg_start=seg_start, used=used, bias=bias, dtype=dtype, num_kv_heads=num_kv_heads,
+                            page_size=page_size, topk=topk, bs=bs, local=local)
+
+
+def dash_paged_n256() -> PagedSegmentCase:
+    """256 decode queries, each attending 8 gathered blocks of 64 keys plus the
+    last up-to-128 keys of its own request (L ~ U[1024, 4096]) in a paged cache."""
+    return paged_segment_case(name="dash_paged_n256", n=256, seed=SEED_BASE + 6)
+
+
 def dash_segments_n256() -> SegmentCase:
     return segment_case(name="dash_segments_n256", seed=WORKLOAD_SEEDS["dash_segments_n256"])
+
+
+@dataclasses.dataclass
+class CacheWriteCase:
+    """A batch of new key/value rows and the paged cache they are written into."""
+    name: str
+    key: np.ndarray        # [T, Hkv, D] storage (in_dtype)
+    value: np.ndarray      # [T, Hkv, D]
+    slots: np.ndarray      # int64 [T]; -1 marks a padding token
+    kv_cache: np.ndarray   # [num_pages, Hkv, P, 2*D] storage (kv_dtype)
+    in_dtype: str
+    kv_dtype: str
+    page_size: int
+    k_scale: float = 1.0
+    v_scale: float = 1.0
+
+    @property
+    def num_tokens(self):
+        return int(self.slots.shape[0])
+
+
+def cache_write_case(*, name="cache_write", num_tokens, num_kv_heads=8, head_dim=128, page_size=16,
+                     in_dtype="bf16", kv_dtype="fp8", seed=0, pool_factor=1.25, pad_every=0) -> CacheWriteCase:
+    """num_tokens new rows written to distinct slots of whole pages drawn in
+    seeded random order from a pool pool_factor times larger than needed."""
+    rng = np.random.default_rng(seed)
+    pages_needed = -(-num_tokens // page_size)
+    num_pages = max(1, int(math.ceil(pool_factor * pages_needed)))
+    pages = rng.permutation(num_pages)[:pages_needed].astype(np.int64)
+    t = np.arange(num_tokens)
+    slots = pages[t // page_size] * page_size + t % page_size
+    if pad_every:
+        slots[::pad_every] = -1
+    key = normal_storage(rng, (num_tokens, num_kv_heads, head_dim), in_dtype)
+    value = normal_storage(rng, (num_tokens, num_kv_heads, head_dim), in_dtype)
+    cache = np.zeros((num_pages, num_kv_heads, page_size, 2 * head_dim), dtype=storage_dtype(kv_dtype))
+    scale = FP8_SCALE if kv_dtype == "fp8" else 1.0
+    return CacheWriteCase(name=name, key=key, value=value, slots=slots, kv_cache=cache, in_dtype=in_dtype,
+                          kv_dtype=kv_dtype, page_size=page_size, k_scale=scale, v_scale=scale)
+
+
+def kv_write_32k() -> CacheWriteCase:
+    """32768 new tokens (a prefill chunk), Hkv=8, D=128, bf16 rows into an fp8 cache, P=16."""
+    return cache_write_case(name="kv_write_32k", num_tokens=32768, seed=SEED_BASE + 5)
 
 
 def to_torch(a: np.ndarray, dtype: str, device="cuda") -> torch.Tensor:
@@ -291,4 +396,6 @@ WORKLOADS = {
     "query_block_sq8_w4096": lambda: query_block_sq8(window=4096),
     "dash_segments_n256": dash_segments_n256,
     "fp8_long_b8": fp8_long_b8,
+    "kv_write_32k": kv_write_32k,
+    "dash_paged_n256": dash_paged_n256,
 }
