@@ -69,7 +69,13 @@ pkd_status make_plan(int B, int sq, int Hq, int Hkv, int D, int P, int max_kv_le
     pl.G = Hq / Hkv;
     pl.M = sq * pl.G;
     const int M = pl.M;
-    pl.flat = B <= pkd::kFlatMaxBatch && !(flags & PKD_FLAG_GRID);
+    // The persistent flat partition balances few or long units best and is the
+    // only home of the fp8 tensor-core warp and of the split row tiles (M > 16);
+    // with many short units of a 16-bit cache and M <= 16 the chunked grid is
+    // faster (gqa_decode_b64: 108.6 vs 126.9 us).  PKD_FLAG_GRID forces the grid.
+    const bool many_units = (long long)B * Hkv >= 256;
+    const bool flat_only = kv == PKD_FP8_E4M3 || (long long)sq * (Hq / Hkv) > 16;
+    pl.flat = B <= pkd::kFlatMaxBatch && !(flags & PKD_FLAG_GRID) && (flat_only || !many_units);
     if (kv == PKD_FP8_E4M3 && (!pl.flat || (flags & PKD_FLAG_FMA))) {
         // the chunked grid reads fp8 on CUDA cores only
         if (M > 8) return fail(PKD_EUNSUPPORTED, "fp8 on CUDA cores supports sq*num_heads/num_kv_heads <= 8 (got %d)", M);

@@ -4,7 +4,8 @@
 // Each warp moves kItemsPerWarp (token, kv head) rows; lanes 0-15 move key
 // rows, lanes 16-31 value rows, 16 input bytes each, all loads issued first.  A 16-bit cache receives the input bits; an
 // fp8 cache receives e4m3(x / scale) rounded to nearest even with saturation
-// (cvt.rn.satfinite), the quotient an IEEE fp32 division.
+// (cvt.rn.satfinite), the quotient an IEEE fp32 division (a multiply by the
+// exact reciprocal when the scale is a power of two: the same rounded value).
 #include "launch.h"
 #include "ptx.cuh"
 
@@ -18,7 +19,13 @@ struct CacheWriteParams {
     long long T, key_stride, value_stride, num_pages;
     int Hkv, D, P, in_elt, kv_elt, in_bf16;
     float k_scale, v_scale;
+    float k_inv, v_inv;  // 1/scale when that scale is a power of two (then x*inv == x/scale exactly), else 0
 };
+
+// x / scale rounded to nearest: a multiply when the reciprocal is exact
+__device__ __forceinline__ float scaled(float x, float scale, float inv) {
+    return inv != 0.f ? x * inv : __fdiv_rn(x, scale);
+}
 
 __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
     uint16_t r;
@@ -35,24 +42,34 @@ __global__ void __launch_bounds__(128) cache_write_kernel(const CacheWriteParams
     const int chunks = p.D * p.in_elt / 16;
     const long long total = p.T * p.Hkv;
     uint4 v[kItemsPerWarp];
+    long long slot[kItemsPerWarp];
     uint8_t* dst[kItemsPerWarp];
+    // every load first (rows and slots are independent), then the stores
 #pragma unroll
     for (int it = 0; it < kItemsPerWarp; ++it) {
-        dst[it] = nullptr;
         const long long wid = w0 + it;
+        slot[it] = -1;
         if (wid >= total || c >= chunks) continue;
-        const long long t = wid / p.Hkv;
+        const long long t = wid / p.Hkv;  // consecutive rows: the kv heads of one token, then the next token
         const int h = static_cast<int>(wid % p.Hkv);
-        const long long s = p.slots[t];
-        if (s < 0 || s / p.P >= p.num_pages) continue;
-        const long long page = s / p.P, off = s % p.P;
         const uint8_t* src = (part ? p.value + (t * p.value_stride + static_cast<long long>(h) * p.D) * p.in_elt
                                    : p.key + (t * p.key_stride + static_cast<long long>(h) * p.D) * p.in_elt) +
                              c * 16;
         v[it] = __ldg(reinterpret_cast<const uint4*>(src));
+        slot[it] = __ldg(p.slots + t);
+    }
+#pragma unroll
+    for (int it = 0; it < kItemsPerWarp; ++it) {
+        dst[it] = nullptr;
+        const long long s = slot[it];
+        if (s < 0 || s / p.P >= p.num_pages) continue;
+        const long long wid = w0 + it;
+        const int h = static_cast<int>(wid % p.Hkv);
+        const long long page = s / p.P, off = s % p.P;
         dst[it] = p.cache + (((page * p.Hkv + h) * p.P + off) * 2 * p.D + part * p.D) * p.kv_elt;
     }
     const float scale = part ? p.v_scale : p.k_scale;
+    const float inv = part ? p.v_inv : p.k_inv;
 #pragma unroll
     for (int it = 0; it < kItemsPerWarp; ++it) {
         if (!dst[it]) continue;
@@ -72,8 +89,8 @@ __global__ void __launch_bounds__(128) cache_write_kernel(const CacheWriteParams
                 f16x2_to_f32(w[2 * i], f[0], f[1]);
                 f16x2_to_f32(w[2 * i + 1], f[2], f[3]);
             }
-            out[i] = f32x2_to_e4m3x2(__fdiv_rn(f[0], scale), __fdiv_rn(f[1], scale)) |
-                     (f32x2_to_e4m3x2(__fdiv_rn(f[2], scale), __fdiv_rn(f[3], scale)) << 16);
+            out[i] = f32x2_to_e4m3x2(scaled(f[0], scale, inv), scaled(f[1], scale, inv)) |
+                     (f32x2_to_e4m3x2(scaled(f[2], scale, inv), scaled(f[3], scale, inv)) << 16);
         }
         *reinterpret_cast<uint2*>(dst[it] + c * 8) = make_uint2(out[0], out[1]);
     }
@@ -100,6 +117,14 @@ cudaError_t launch_cache_write(const void* key, const void* value, int in_dtype,
     p.in_bf16 = in_dtype == 0;
     p.k_scale = k_scale;
     p.v_scale = v_scale;
+    // a power-of-two scale has an exact reciprocal (within the normal range)
+    auto exact_inv = [](float s) {
+        int e;
+        const float m = frexpf(s, &e);
+        return (m == 0.5f && e > -120 && e < 120) ? 1.0f / s : 0.0f;
+    };
+    p.k_inv = exact_inv(k_scale);
+    p.v_inv = exact_inv(v_scale);
     const long long warps = (T * Hkv + kItemsPerWarp - 1) / kItemsPerWarp;
     if (warps == 0) return cudaSuccess;
     cache_write_kernel<<<static_cast<unsigned>((warps + 3) / 4), 128, 0, stream>>>(p);

@@ -50,7 +50,65 @@ struct StageMeta {
     int b, hk, s, page;
 };
 
-template <class W, int D, int ELT, int NBUF>
+// Merge the partials of unit (b, hk) left by workers wf..wl (the caller is the
+// last to arrive).  Two passes of independent loads: per-row max and sum of
+// weights, then float4 sums.  Out of line: it runs once per shared unit.
+template <int D>
+__device__ __noinline__ void merge_unit(const DecodeParams& p, int b, int hk, long long wf, long long wl,
+                                        long long Stot, long long Weff, long long E, float* mstat, int lane) {
+    auto slot = [&](long long v) { return v * 2 + ((v + 1) * Stot / Weff < E ? 1 : 0); };
+    float* smx = mstat;
+    float* sinv = mstat + 32;
+    for (int r = lane; r < p.M; r += 32) {
+        float mx = -INFINITY;
+#pragma unroll 4
+        for (long long v = wf; v <= wl; ++v) mx = fmaxf(mx, __ldcg(p.part_lse + slot(v) * p.M + r));
+        float ws = 0.f;
+        if (mx != -INFINITY) {
+#pragma unroll 4
+            for (long long v = wf; v <= wl; ++v) {
+                const float lc = __ldcg(p.part_lse + slot(v) * p.M + r);
+                ws += lc == -INFINITY ? 0.f : fast_exp2(lc - mx);
+            }
+        }
+        smx[r] = mx;
+        sinv[r] = ws > 0.f ? 1.f / ws : 0.f;
+        if (p.lse) {
+            const int i = r / p.G, g = r % p.G;
+            p.lse[(static_cast<long long>(b) * p.sq + i) * p.Hq + hk * p.G + g] =
+                ws > 0.f ? (mx + __log2f(ws)) * kLn2 : -INFINITY;
+        }
+    }
+    __syncwarp();
+    for (int q4 = lane; q4 < p.M * D / 4; q4 += 32) {
+        const int r = (q4 * 4) / D, d = (q4 * 4) % D;
+        const float mx = smx[r], inv = sinv[r];
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (inv > 0.f) {
+#pragma unroll 4
+            for (long long v = wf; v <= wl; ++v) {
+                const long long sl2 = slot(v);
+                const float lc = __ldcg(p.part_lse + sl2 * p.M + r);
+                const float4 o = __ldcg(reinterpret_cast<const float4*>(p.part_out + sl2 * p.M * D) + q4);
+                const float w = lc == -INFINITY ? 0.f : fast_exp2(lc - mx) * inv;  // empty partials hold 0
+                acc.x = fmaf(w, o.x, acc.x);
+                acc.y = fmaf(w, o.y, acc.y);
+                acc.z = fmaf(w, o.z, acc.z);
+                acc.w = fmaf(w, o.w, acc.w);
+            }
+        }
+        const long long oi = out_index(p, b, hk, r, d, D);
+        store_out(p.out, oi, acc.x * p.v_scale, p.out_dtype);
+        store_out(p.out, oi + 1, acc.y * p.v_scale, p.out_dtype);
+        store_out(p.out, oi + 2, acc.z * p.v_scale, p.out_dtype);
+        store_out(p.out, oi + 3, acc.w * p.v_scale, p.out_dtype);
+    }
+}
+
+// RT > 1: the query rows of a unit are split into RT tiles of 16, held by RT
+// consecutive warps that walk the same slice of keys (each with its own ring;
+// the repeated loads of a stage are served by L2).
+template <class W, int D, int ELT, int NBUF, int RT>
 __global__ void __launch_bounds__(kNW * 32)
 decode_flat_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p) {
     using S = FlatShape<D, ELT, NBUF, W::kScratchBytes>;
@@ -119,11 +177,13 @@ decode_flat_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams 
     }
 
     // ---- this warp's slice of the flat stage sequence
-    const long long Wtot = static_cast<long long>(gridDim.x) * kNW;
+    static_assert(kNW % RT == 0, "row-tile groups must not straddle CTAs");
+    const int rt = warp % RT;
+    const long long Wtot = static_cast<long long>(gridDim.x) * (kNW / RT);
     long long Weff = Stot / kFlatMinStages;
     if (Weff > Wtot) Weff = Wtot;
     if (Weff < 1) Weff = 1;
-    const long long wid = static_cast<long long>(blockIdx.x) * kNW + warp;
+    const long long wid = (static_cast<long long>(blockIdx.x) * kNW + warp) / RT;
     if (Stot == 0 || wid >= Weff) return;
     const long long f0 = wid * Stot / Weff, f1 = (wid + 1) * Stot / Weff;
     const int n = static_cast<int>(f1 - f0);
@@ -194,7 +254,7 @@ decode_flat_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams 
     StageMeta cur = fetch(f0 + lane), nxt = fetch(f0 + 32 + lane);
     for (int k = NBUF; k < NBUF + kPrefetch; ++k) {
         const StageMeta m = shfl_meta(cur, k);
-        if (lane == 0 && k < n) prefetch(m);
+        if (lane == 0 && k < n && rt == 0) prefetch(m);
     }
     for (int k = 0; k < NBUF && k < n; ++k) {
         const StageMeta m = shfl_meta(cur, k);
@@ -204,6 +264,8 @@ decode_flat_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams 
     W wp;
     wp.init(lane);
     wp.setup(smem + S::OFF_SCR + warp * W::kScratchBytes);
+    wp.row0 = rt * 16;
+    const int row0 = wp.row0;
     int ub = -1, uh = -1, uL = 0, ulo = 0, ucnt = 0;
 
     // finish unit (ub, uh): direct write, or partial + last-arriver merge
@@ -215,10 +277,12 @@ decode_flat_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams 
         const int b = ub, hk = uh;
         if (wf == wl) {
             wp.emit([&](int r, int d, float v) {
+                r += row0;
                 if (r < p.M) store_out(p.out, out_index(p, b, hk, r, d, D), v * p.v_scale, p.out_dtype);
             }, lane);
             if (p.lse)
                 wp.emit_lse([&](int r, float l2) {
+                    r += row0;
                     if (r < p.M) {
                         const int i = r / p.G, g = r % p.G;
                         p.lse[(static_cast<long long>(b) * p.sq + i) * p.Hq + hk * p.G + g] = l2 * kLn2;
@@ -229,79 +293,31 @@ decode_flat_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams 
         const int side = f1 < E ? 1 : 0;  // 1: the unit continues past this slice
         float* so = p.part_out + (wid * 2 + side) * p.M * D;
         float* sl = p.part_lse + (wid * 2 + side) * p.M;
-        wp.emit([&](int r, int d, float v) { if (r < p.M) __stcg(so + r * D + d, v); }, lane);
-        wp.emit_lse([&](int r, float l2) { if (r < p.M) __stcg(sl + r, l2); }, lane);
+        wp.emit([&](int r, int d, float v) { r += row0; if (r < p.M) __stcg(so + r * D + d, v); }, lane);
+        wp.emit_lse([&](int r, float l2) { r += row0; if (r < p.M) __stcg(sl + r, l2); }, lane);
         __threadfence();
         __syncwarp();
         const int u = b * p.Hkv + hk;
         int last = 0;
         if (lane == 0) {
             const int prev = atomicAdd(p.counters + u, 1);
-            last = prev == static_cast<int>(wl - wf);
+            last = prev == static_cast<int>((wl - wf + 1) * RT - 1);
             if (last) atomicExch(p.counters + u, 0);  // ready for the next call
         }
         last = __shfl_sync(kFull, last, 0);
         if (!last) return;
         __threadfence();
-        // merge the partials of workers wf..wl; every load of a pass is
-        // independent, so a pass costs about one L2 round trip
-        auto slot = [&](long long v) { return v * 2 + ((v + 1) * Stot / Weff < E ? 1 : 0); };
-        float* smx = mstat;
-        float* sinv = mstat + 32;
-        for (int r = lane; r < p.M; r += 32) {
-            float mx = -INFINITY;
-#pragma unroll 4
-            for (long long v = wf; v <= wl; ++v) mx = fmaxf(mx, __ldcg(p.part_lse + slot(v) * p.M + r));
-            float ws = 0.f;
-            if (mx != -INFINITY) {
-#pragma unroll 4
-                for (long long v = wf; v <= wl; ++v) {
-                    const float lc = __ldcg(p.part_lse + slot(v) * p.M + r);
-                    ws += lc == -INFINITY ? 0.f : fast_exp2(lc - mx);
-                }
-            }
-            smx[r] = mx;
-            sinv[r] = ws > 0.f ? 1.f / ws : 0.f;
-            if (p.lse) {
-                const int i = r / p.G, g = r % p.G;
-                p.lse[(static_cast<long long>(b) * p.sq + i) * p.Hq + hk * p.G + g] =
-                    ws > 0.f ? (mx + __log2f(ws)) * kLn2 : -INFINITY;
-            }
-        }
-        __syncwarp();
-        for (int q4 = lane; q4 < p.M * D / 4; q4 += 32) {
-            const int r = (q4 * 4) / D, d = (q4 * 4) % D;
-            const float mx = smx[r], inv = sinv[r];
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (inv > 0.f) {
-#pragma unroll 4
-                for (long long v = wf; v <= wl; ++v) {
-                    const long long sl2 = slot(v);
-                    const float lc = __ldcg(p.part_lse + sl2 * p.M + r);
-                    const float4 o = __ldcg(reinterpret_cast<const float4*>(p.part_out + sl2 * p.M * D) + q4);
-                    const float w = lc == -INFINITY ? 0.f : fast_exp2(lc - mx) * inv;  // empty partials hold 0
-                    acc.x = fmaf(w, o.x, acc.x);
-                    acc.y = fmaf(w, o.y, acc.y);
-                    acc.z = fmaf(w, o.z, acc.z);
-                    acc.w = fmaf(w, o.w, acc.w);
-                }
-            }
-            const long long oi = out_index(p, b, hk, r, d, D);
-            store_out(p.out, oi, acc.x * p.v_scale, p.out_dtype);
-            store_out(p.out, oi + 1, acc.y * p.v_scale, p.out_dtype);
-            store_out(p.out, oi + 2, acc.z * p.v_scale, p.out_dtype);
-            store_out(p.out, oi + 3, acc.w * p.v_scale, p.out_dtype);
-        }
+        merge_unit<D>(p, b, hk, wf, wl, Stot, Weff, E, mstat, lane);
         __syncwarp();
     };
 
     for (int k = 0; k < n; ++k) {
-        if (k > 0 && (k & 31) == 0) {
+        if (__builtin_expect(k > 0 && (k & 31) == 0, 0)) {
             cur = nxt;
             nxt = fetch(f0 + k + 32 + lane);
         }
         const StageMeta mk = shfl_meta(cur, k & 31);
-        if (mk.b != ub || mk.hk != uh) {
+        if (__builtin_expect(mk.b != ub || mk.hk != uh, 0)) {
             if (ub >= 0) finalize();
             ub = mk.b;
             uh = mk.hk;
@@ -312,7 +328,7 @@ decode_flat_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams 
             wp.load_q(p, ub, uh, lane);
         }
         const int buf = k % NBUF;
-        if (!mbar_wait(bar0 + 8 * buf, (k / NBUF) & 1, p.status)) {
+        if (__builtin_expect(!mbar_wait(bar0 + 8 * buf, (k / NBUF) & 1, p.status), 0)) {
             if (lane == 0) raise_status(p, kErrTimeout);
             for (int j = k + 1; j < n && j < k + NBUF; ++j) mbar_wait(bar0 + 8 * (j % NBUF), (j / NBUF) & 1, p.status);
             return;
@@ -323,7 +339,7 @@ decode_flat_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams 
         uint8_t* st_gen = ring_gen + buf * S::STAGE;
         if (nvalid < kStageTok) zero_tail_v<D, ELT>(st_gen, nvalid, lane);
         const int L = uL;
-        auto visible = [&](int row, int kt) { return row_sees(p, L, row, tok0 + kt); };
+        auto visible = [&](int row, int kt) { return row_sees(p, L, row0 + row, tok0 + kt); };
         if constexpr (W::kTensor)
             wp.consume(ring + buf * S::STAGE, S::HALF, nvalid, nvalid < kStageTok || p.causal, p.scale_log2, 0.f,
                        visible, lane);
@@ -334,9 +350,10 @@ decode_flat_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams 
         if (j < n) {
             const StageMeta mj = shfl_meta((j >> 5) == (k >> 5) ? cur : nxt, j & 31);
             const int jp = j + kPrefetch;
-            const StageMeta mp = shfl_meta((jp >> 5) == (k >> 5) ? cur : nxt, jp & 31);
+            StageMeta mp;
+            if (kPrefetch > 0) mp = shfl_meta((jp >> 5) == (k >> 5) ? cur : nxt, jp & 31);
             if (lane == 0) {
-                if (jp < n) prefetch(mp);
+                if (kPrefetch > 0 && jp < n && rt == 0) prefetch(mp);
                 fence_proxy_async();
                 issue(j, mj);
             }

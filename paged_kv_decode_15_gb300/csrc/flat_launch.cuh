@@ -7,10 +7,10 @@
 
 namespace pkd {
 
-template <class W, int D, int ELT>
+template <class W, int D, int ELT, int RT = 1>
 cudaError_t launch_flat_one(const CUtensorMap& tmap, const DecodeParams& p, int max_ctas, cudaStream_t stream) {
     using S = FlatShape<D, ELT, W::kNbuf, W::kScratchBytes>;
-    auto kern = decode_flat_kernel<W, D, ELT, W::kNbuf>;
+    auto kern = decode_flat_kernel<W, D, ELT, W::kNbuf, RT>;
     static int per_sm = 0;  // benign race: every thread computes the same value
     if (per_sm == 0) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);

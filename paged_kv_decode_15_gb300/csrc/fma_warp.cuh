@@ -79,6 +79,7 @@ struct FmaWarp {
     float acc[MR][EPL];
     float m_run, l_run;
     int myrow;
+    int row0 = 0;  // row tiles are never split across CUDA-core warps (M <= 8)
 
     // head-dimension index of lane segment s, element e
     __device__ __forceinline__ static int dim_of(int j, int s, int e) { return (j + LPT * s) * EPS + e; }

@@ -34,7 +34,7 @@ struct Fp8MmaWarp : MmaWarp<128, false, MT, NT> {
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                const int r = mt * 16 + h * 8 + g;
+                const int r = this->row0 + mt * 16 + h * 8 + g;
                 const uint32_t* row = nullptr;
                 if (r < p.M) {
                     const int i = r / p.G, gg = r % p.G;

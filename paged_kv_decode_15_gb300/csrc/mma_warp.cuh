@@ -22,6 +22,7 @@ struct MmaWarp {
     uint32_t qa[kQSmem ? 1 : MT][D / 16][4];
     uint32_t qs = 0;
     uint8_t* qs_gen = nullptr;
+    int row0 = 0;  // first query row of (b, hk) this warp holds (row tiles split across warps)
     float m_run[MT][2], l_run[MT][2];
     float oacc[D / 16][NT][4];
 
@@ -101,7 +102,7 @@ struct MmaWarp {
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                const int r = mt * 16 + h * 8 + g;
+                const int r = row0 + mt * 16 + h * 8 + g;
                 const uint32_t* row = nullptr;
                 if (r < p.M) {
                     const int i = r / p.G, gg = r % p.G;

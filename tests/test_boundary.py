@@ -48,10 +48,17 @@ def test_workspace_plan_is_a_host_function(lib):
     # chunked grid, explicit chunk: 4096 / 256 = 16 splits -> partials [512 units, 16, 4 rows, 128] fp32
     m = pkd.workspace_size(64, 1, 32, 8, 128, 16, 4096, pkd.BF16, chunk_tokens=256, flags=pkd.FLAG_GRID)
     assert m >= 512 * 16 * 4 * 128 * 4
-    # flat partition: two partial slots per worker warp, independent of the lengths
-    f1 = pkd.workspace_size(64, 1, 32, 8, 128, 16, 4096, pkd.BF16)
-    f2 = pkd.workspace_size(64, 1, 32, 8, 128, 16, 131072, pkd.BF16)
+    # flat partition (few units: 8 x 8 < 256): two partial slots per worker warp, independent of the lengths
+    f1 = pkd.workspace_size(8, 1, 32, 8, 128, 16, 4096, pkd.BF16)
+    f2 = pkd.workspace_size(8, 1, 32, 8, 128, 16, 131072, pkd.BF16)
     assert f1 == f2 and f1 >= 2048 * 2 * 4 * 128 * 4
+    # many short units of a 16-bit cache with M <= 16 take the chunked grid by default ...
+    assert n == pkd.workspace_size(64, 1, 32, 8, 128, 16, 4096, pkd.BF16, flags=pkd.FLAG_GRID)
+    # ... and fp8 or M > 16 stay on the flat partition whatever the batch
+    assert pkd.workspace_size(64, 1, 32, 8, 128, 16, 4096, pkd.FP8_E4M3) == \
+        pkd.workspace_size(64, 1, 32, 8, 128, 16, 131072, pkd.FP8_E4M3)
+    assert pkd.workspace_size(64, 8, 32, 8, 128, 16, 4096, pkd.BF16) == \
+        pkd.workspace_size(64, 8, 32, 8, 128, 16, 131072, pkd.BF16)
     # batches above the flat kernel's table size use the chunked grid
     assert pkd.workspace_size(2048, 1, 32, 8, 128, 16, 4096, pkd.BF16) == \
         pkd.workspace_size(2048, 1, 32, 8, 128, 16, 4096, pkd.BF16, flags=pkd.FLAG_GRID)
