@@ -165,9 +165,8 @@ class PagedRunner:
         self.lse = torch.empty(case.q.shape[:3], dtype=torch.float32, device="cuda")
         self.max_kv_len = int(case.block_table.shape[1] * case.page_size)
         kv_code = {"bf16": pkd.BF16, "fp16": pkd.FP16, "fp8": pkd.FP8_E4M3}[case.dtype]
-        self.chunk, self.path, self.grid = args.chunk, args.path, args.grid
-        flags = (pkd.FLAG_CAUSAL if case.causal else 0) | (pkd.FLAG_FMA if self.path == "fma" else 0) | \
-            (pkd.FLAG_GRID if self.grid else 0)
+        self.chunk, self.path, self.grid, self.flat = args.chunk, args.path, args.grid, args.flat
+        flags = paged_flags(case, args, pkd)
         self.ws = torch.empty(pkd.workspace_size(case.batch, case.sq, case.num_heads, case.num_kv_heads,
                                                  case.head_dim, case.page_size, self.max_kv_len, kv_code, case.window,
                                                  self.chunk, flags), dtype=torch.uint8, device="cuda")
@@ -181,7 +180,7 @@ class PagedRunner:
         self.pkd.paged_decode(self.q, self.cache, self.bt, self.lens, c.scale, c.window, out=self.out, lse=self.lse,
                               q_scale=c.q_scale, k_scale=c.k_scale, v_scale=c.v_scale, max_kv_len=self.max_kv_len,
                               workspace=self.ws, causal=c.causal, chunk_tokens=self.chunk,
-                              force_fma=self.path == "fma", grid=self.grid)
+                              force_fma=self.path == "fma", grid=self.grid, flat=self.flat)
 
     def check(self):
         if self.pkd.workspace_check(self.ws) != self.pkd.OK:
@@ -290,7 +289,19 @@ def run_gpu(args, rank, world, dist):
         CacheWriteRunner if isinstance(case, wl.CacheWriteCase) else \
         PagedSegmentRunner if isinstance(case, wl.PagedSegmentCase) else PagedRunner
     runner = kind(case, args, torch, pkd)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    words = flush_buf.view(torch.int32)
+
+    class _Flush:
+        """Evict L2 before a step: write a buffer larger than L2; with
+        write-read, then read half of it back so that L2 holds clean lines and
+        no write-back of the flush is left to compete with the step."""
+        @staticmethod
+        def zero_():
+            flush_buf.zero_()
+            if args.l2_flush == "write-read":
+                words[:words.numel() // 2].amax()
+    flush = _Flush()
     stream = torch.cuda.current_stream()
 
     for _ in range(args.warmup):
@@ -427,27 +438,49 @@ def workload_config(case, args) -> dict:
     if hasattr(case, "slots"):
         return {"workload": case.name, "num_tokens": case.num_tokens, "num_kv_heads": case.key.shape[1],
                 "head_dim": case.key.shape[2], "page_size": case.page_size, "in_dtype": case.in_dtype,
-                "kv_dtype": case.kv_dtype, "l2": "L2 flushed (512 MiB write) before every timed step"}
+                "kv_dtype": case.kv_dtype, "l2": l2_note(args)}
     if hasattr(case, "seg_start"):
         return {"workload": case.name, "n": case.n, "num_heads": case.q.shape[1], "num_kv_heads": case.num_kv_heads,
                 "head_dim": case.q.shape[2], "page_size": case.page_size, "topk": case.topk, "bs": case.bs,
                 "local": case.local, "dtype": case.dtype, "used_keys": int(case.used.sum()),
-                "l2": "L2 flushed (512 MiB write) before every timed step"}
+                "l2": l2_note(args)}
     if not hasattr(case, "seq_lens"):
         return {"workload": case.name, "n": case.n, "num_heads": case.q.shape[1], "num_kv_heads": case.num_kv_heads,
                 "head_dim": case.q.shape[2], "topk": case.topk, "bs": case.bs, "local": case.local,
                 "dtype": case.dtype, "used_rows": int(case.used.sum()),
-                "l2": "L2 flushed (512 MiB write) before every timed step"}
+                "l2": l2_note(args)}
     return {"workload": case.name, "batch": case.batch, "sq": case.sq, "num_heads": case.num_heads,
             "num_kv_heads": case.num_kv_heads, "head_dim": case.head_dim, "page_size": case.page_size,
             "kv_dtype": case.dtype, "window": case.window, "causal": case.causal,
             "seq_lens": {"min": int(case.seq_lens.min()), "max": int(case.seq_lens.max()),
                          "total": int(case.seq_lens.sum())},
-            "pool_pages": case.num_pages, "l2": "L2 flushed (512 MiB write) before every timed step; "
-                                                "KV stream larger than L2",
+            "pool_pages": case.num_pages, "l2": l2_note(args) + "; KV stream larger than L2",
             "parallelism": f"replicas{args.gpus}" if args.gpus > 1 else "single",
             "kernel_path": getattr(args, "path", "auto"), "chunk_tokens": getattr(args, "chunk", 0),
-            "partition": "chunked grid" if getattr(args, "grid", False) else "persistent flat"}
+            "kernel": paged_kernel_name(case, args)}
+
+
+def paged_flags(case, args, pkd) -> int:
+    return (pkd.FLAG_CAUSAL if case.causal else 0) | (pkd.FLAG_FMA if args.path == "fma" else 0) | \
+        (pkd.FLAG_GRID if args.grid else 0) | (pkd.FLAG_FLAT if args.flat else 0)
+
+
+def paged_kernel_name(case, args) -> str:
+    """The library's own account of the kernel it launches for this workload."""
+    import paged_kv_decode_15_gb300 as pkd
+    try:
+        kv_code = {"bf16": pkd.BF16, "fp16": pkd.FP16, "fp8": pkd.FP8_E4M3}[case.dtype]
+        return pkd.kernel_name(case.batch, case.sq, case.num_heads, case.num_kv_heads, case.head_dim,
+                               case.page_size, int(case.block_table.shape[1] * case.page_size), kv_code,
+                               case.window, args.chunk, paged_flags(case, args, pkd))
+    except (OSError, RuntimeError) as e:  # library not built on this host
+        return f"unknown ({e})"
+
+
+def l2_note(args) -> str:
+    if args.l2_flush == "write-read":
+        return "L2 flushed before every timed step: 512 MiB write, then 256 MiB read (clean lines)"
+    return "L2 flushed (512 MiB write) before every timed step"
 
 
 def main():
@@ -461,8 +494,10 @@ def main():
     ap.add_argument("--chunk", type=int, default=0, help="Split-KV chunk in keys (0 = the library's plan)")
     ap.add_argument("--path", default="auto", choices=["auto", "fma"],
                     help="library default (tensor cores for 16-bit caches) or CUDA cores")
-    ap.add_argument("--grid", action="store_true",
-                    help="one CTA per Split-KV chunk instead of the persistent flat partition")
+    ap.add_argument("--grid", action="store_true", help="force the chunked grid (one CTA per Split-KV chunk)")
+    ap.add_argument("--flat", action="store_true", help="force the persistent flat partition")
+    ap.add_argument("--l2-flush", default="write", choices=["write", "write-read"],
+                    help="how L2 is evicted before every timed step")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -48,6 +48,7 @@ typedef enum {
 #define PKD_FLAG_MMA_SMALL_M 2u /* tensor cores for sq*Hq/Hkv < 16 (the default for 16-bit caches) */
 #define PKD_FLAG_FMA 4u         /* CUDA cores instead (only when sq*Hq/Hkv <= 8; always for fp8) */
 #define PKD_FLAG_GRID 8u        /* one CTA per Split-KV chunk instead of the persistent flat partition */
+#define PKD_FLAG_FLAT 16u       /* the persistent flat partition whatever the shapes (batch <= 1024) */
 
 /* Library version, major*10000 + minor*100 + patch. */
 int pkd_version(void);
@@ -68,6 +69,18 @@ size_t pkd_paged_decode_workspace_size(int batch, int sq, int num_heads, int num
                                        int head_dim, int page_size, int max_kv_len,
                                        pkd_dtype kv_dtype, int window, int chunk_tokens,
                                        unsigned flags);
+
+/*
+ * Which kernel pkd_paged_decode launches for a plan (same arguments as
+ * pkd_paged_decode_workspace_size): a static string such as
+ * "chunked grid, tensor cores".  Host-only, no CUDA call.  Returns NULL for
+ * an invalid request (the reason is in pkd_last_error).  The pages have no
+ * counterpart of this call; it makes the library's choice of kernel visible
+ * to callers and benchmarks.
+ */
+const char* pkd_paged_decode_kernel_name(int batch, int sq, int num_heads, int num_kv_heads, int head_dim,
+                                         int page_size, int max_kv_len, pkd_dtype kv_dtype, int window,
+                                         int chunk_tokens, unsigned flags);
 
 /*
  * Zero a workspace (asynchronously on `stream`).  Needed once, before its

@@ -22,9 +22,10 @@ LIB_PATH = os.path.join(_HERE, "libpkd.so")
 
 OK, EINVAL, EUNSUPPORTED, ECUDA, EDEVICE_BOUNDS, ETIMEOUT = range(6)
 BF16, FP16, FP8_E4M3, FP32 = 0, 1, 2, 3
-FLAG_CAUSAL, FLAG_MMA_SMALL_M, FLAG_FMA, FLAG_GRID = 1, 2, 4, 8
+FLAG_CAUSAL, FLAG_MMA_SMALL_M, FLAG_FMA, FLAG_GRID, FLAG_FLAT = 1, 2, 4, 8, 16
 
-SYMBOLS = ("pkd_version", "pkd_last_error", "pkd_paged_decode_workspace_size", "pkd_workspace_init",
+SYMBOLS = ("pkd_version", "pkd_last_error", "pkd_paged_decode_workspace_size", "pkd_paged_decode_kernel_name",
+           "pkd_workspace_init",
            "pkd_workspace_check", "pkd_paged_decode", "pkd_paged_decode_static", "pkd_cache_write",
            "pkd_segmented_attention", "pkd_segmented_attention_paged", "pkd_lse_merge")
 
@@ -59,6 +60,8 @@ def load_library(path: str = LIB_PATH):
     lib.pkd_last_error.restype = ctypes.c_char_p
     lib.pkd_paged_decode_workspace_size.argtypes = [I, I, I, I, I, I, I, I, I, I, U]
     lib.pkd_paged_decode_workspace_size.restype = SZ
+    lib.pkd_paged_decode_kernel_name.argtypes = [I, I, I, I, I, I, I, I, I, I, U]
+    lib.pkd_paged_decode_kernel_name.restype = ctypes.c_char_p
     lib.pkd_workspace_init.argtypes = [P, SZ, P]
     lib.pkd_workspace_check.argtypes = [P, SZ, P]
     lib.pkd_paged_decode.argtypes = [P, I, P, I, I64, P, I64, P, I, I, I, I, I, I, I, F, F, F, F, I,
@@ -123,6 +126,17 @@ def workspace_size(batch, sq, num_heads, num_kv_heads, head_dim, page_size, max_
     return n
 
 
+def kernel_name(batch, sq, num_heads, num_kv_heads, head_dim, page_size, max_kv_len, kv_dtype, window=0,
+                chunk_tokens=0, flags=0) -> str:
+    """The kernel paged_decode launches for these shapes and flags."""
+    name = load_library().pkd_paged_decode_kernel_name(batch, sq, num_heads, num_kv_heads, head_dim, page_size,
+                                                       max_kv_len, int(kv_dtype), int(window), int(chunk_tokens),
+                                                       int(flags))
+    if name is None:
+        raise PkdError(EINVAL, load_library().pkd_last_error().decode())
+    return name.decode()
+
+
 def workspace_init(ws: torch.Tensor, stream=None):
     _check(load_library().pkd_workspace_init(_ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
@@ -147,7 +161,7 @@ def _workspace(nbytes: int, device) -> torch.Tensor:
 
 def paged_decode(q, kv_cache, block_table, seq_lens, scale, window=0, out=None, lse=None, *, q_scale=1.0,
                  k_scale=1.0, v_scale=1.0, max_kv_len=None, workspace=None, chunk_tokens=0, causal=False,
-                 mma_small_m=False, force_fma=False, grid=False, out_dtype=None, stream=None):
+                 mma_small_m=False, force_fma=False, grid=False, flat=False, out_dtype=None, stream=None):
     """Attention of each request's query block over its paged keys.
 
     q [B, sq, Hq, D]; kv_cache [num_pages, Hkv, P, 2*D] (bf16, fp16, or uint8 /
@@ -178,7 +192,7 @@ def paged_decode(q, kv_cache, block_table, seq_lens, scale, window=0, out=None, 
     if max_kv_len is None:
         max_kv_len = block_table.shape[1] * P
     flags = (FLAG_CAUSAL if causal else 0) | (FLAG_MMA_SMALL_M if mma_small_m else 0) | \
-        (FLAG_FMA if force_fma else 0) | (FLAG_GRID if grid else 0)
+        (FLAG_FMA if force_fma else 0) | (FLAG_GRID if grid else 0) | (FLAG_FLAT if flat else 0)
     need = workspace_size(B, sq, Hq, Hkv, D, P, max_kv_len, kv_dt, window, chunk_tokens, flags)
     if workspace is None:
         workspace = _workspace(need, q.device)

@@ -75,7 +75,10 @@ pkd_status make_plan(int B, int sq, int Hq, int Hkv, int D, int P, int max_kv_le
     // faster (gqa_decode_b64: 108.6 vs 126.9 us).  PKD_FLAG_GRID forces the grid.
     const bool many_units = (long long)B * Hkv >= 256;
     const bool flat_only = kv == PKD_FP8_E4M3 || (long long)sq * (Hq / Hkv) > 16;
-    pl.flat = B <= pkd::kFlatMaxBatch && !(flags & PKD_FLAG_GRID) && (flat_only || !many_units);
+    if ((flags & PKD_FLAG_GRID) && (flags & PKD_FLAG_FLAT))
+        return fail(PKD_EINVAL, "PKD_FLAG_GRID and PKD_FLAG_FLAT exclude each other");
+    pl.flat = B <= pkd::kFlatMaxBatch && !(flags & PKD_FLAG_GRID) &&
+              ((flags & PKD_FLAG_FLAT) || flat_only || !many_units);
     if (kv == PKD_FP8_E4M3 && (!pl.flat || (flags & PKD_FLAG_FMA))) {
         // the chunked grid reads fp8 on CUDA cores only
         if (M > 8) return fail(PKD_EUNSUPPORTED, "fp8 on CUDA cores supports sq*num_heads/num_kv_heads <= 8 (got %d)", M);
@@ -276,6 +279,17 @@ size_t pkd_paged_decode_workspace_size(int batch, int sq, int num_heads, int num
                   chunk_tokens, flags, pl) != PKD_OK)
         return 0;
     return pl.bytes;
+}
+
+const char* pkd_paged_decode_kernel_name(int batch, int sq, int num_heads, int num_kv_heads, int head_dim,
+                                         int page_size, int max_kv_len, pkd_dtype kv_dtype, int window,
+                                         int chunk_tokens, unsigned flags) {
+    Plan pl;
+    if (make_plan(batch, sq, num_heads, num_kv_heads, head_dim, page_size, max_kv_len, kv_dtype, window,
+                  chunk_tokens, flags, pl) != PKD_OK)
+        return nullptr;
+    if (pl.flat) return pl.mma ? "persistent flat partition, tensor cores" : "persistent flat partition, CUDA cores";
+    return pl.mma ? "chunked grid, tensor cores" : "chunked grid, CUDA cores";
 }
 
 pkd_status pkd_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {

@@ -138,3 +138,18 @@ def test_lse_merge_validation(lib):
     assert m(None, None, None, None, 0, 4, 2, 64, None, pkd.FP32, None, None) == pkd.OK
     assert m(None, None, None, None, 3, 4, 2, 64, None, pkd.FP32, None, None) == pkd.EINVAL
     assert m(None, None, None, None, 3, 4, 2, 512, None, pkd.FP32, None, None) == pkd.EUNSUPPORTED
+
+
+def test_kernel_name_follows_the_plan(lib):
+    args = (64, 1, 32, 8, 128, 16, 4096)
+    assert pkd.kernel_name(*args, pkd.BF16) == "chunked grid, tensor cores"
+    assert pkd.kernel_name(*args, pkd.BF16, flags=pkd.FLAG_FLAT) == "persistent flat partition, tensor cores"
+    assert pkd.kernel_name(8, 1, 32, 8, 128, 16, 4096, pkd.BF16) == "persistent flat partition, tensor cores"
+    assert pkd.kernel_name(*args, pkd.BF16, flags=pkd.FLAG_FMA | pkd.FLAG_GRID) == "chunked grid, CUDA cores"
+    assert pkd.kernel_name(*args, pkd.FP8_E4M3) == "persistent flat partition, tensor cores"
+    assert pkd.kernel_name(*args, pkd.FP8_E4M3, flags=pkd.FLAG_GRID) == "chunked grid, CUDA cores"
+    assert pkd.kernel_name(2048, 1, 32, 8, 128, 16, 4096, pkd.FP8_E4M3) == "chunked grid, CUDA cores"
+    with pytest.raises(pkd.PkdError, match="head_dim"):
+        pkd.kernel_name(2, 1, 8, 2, 96, 16, 100, pkd.BF16)
+    with pytest.raises(pkd.PkdError, match="exclude"):
+        pkd.kernel_name(*args, pkd.BF16, flags=pkd.FLAG_FLAT | pkd.FLAG_GRID)
