@@ -5,8 +5,9 @@
 A step is one paged_decode call over the workload's whole batch (window
 restriction, page gather, logits, online softmax, P.V, Split-KV merge and
 epilogue, all in one kernel launch).  Inputs are resident in HBM; the L2 is
-flushed (a 512 MiB write) before every timed step and the KV stream is larger
-than the L2 anyway.  Each step is timed with CUDA events on the launching
+flushed before every timed step (a 512 MiB write, then a 256 MiB read so that
+no dirty line of the flush is written back inside the step; --l2-flush write
+keeps only the write) and the KV stream is larger than the L2 anyway.  Each step is timed with CUDA events on the launching
 stream; value = algorithmic KV bytes of all ranks / max over ranks of the
 summed step time.  One JSON line is printed by rank 0.
 
@@ -496,8 +497,10 @@ def main():
                     help="library default (tensor cores for 16-bit caches) or CUDA cores")
     ap.add_argument("--grid", action="store_true", help="force the chunked grid (one CTA per Split-KV chunk)")
     ap.add_argument("--flat", action="store_true", help="force the persistent flat partition")
-    ap.add_argument("--l2-flush", default="write", choices=["write", "write-read"],
-                    help="how L2 is evicted before every timed step")
+    ap.add_argument("--l2-flush", default="write-read", choices=["write", "write-read"],
+                    help="how L2 is evicted before every timed step: a 512 MiB write (it leaves up to an L2 of "
+                         "dirty lines whose write-back lands inside the timed step), or that write followed by a "
+                         "256 MiB read that leaves L2 holding clean, unrelated lines")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -40,7 +40,11 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 int elt_bytes(pkd_dtype dt) { return dt == PKD_FP8_E4M3 ? 1 : dt == PKD_FP32 ? 4 : 2; }
 
 // ---------------------------------------------------------------- plan
-constexpr int kTargetCtas = 1024;  // Split-KV aims for about this many live CTAs
+// Split-KV aims for about this many CTAs: measured on gqa_decode_b64 (M = 4)
+// 2048 (1024-key chunks) beats 1024, 1536 or 3072; the warp-pair kernel
+// (M > 16) does better with half as many, longer chunks.
+constexpr int kTargetCtas = 2048;
+constexpr int kTargetCtasPair = 1024;
 constexpr int kMaxChunk = 4096;    // and never puts more keys than this in one chunk
 constexpr size_t kHeader = 256;    // workspace status word lives in the first bytes
 
@@ -110,7 +114,8 @@ pkd_status make_plan(int B, int sq, int Hq, int Hkv, int D, int P, int max_kv_le
             return fail(PKD_EINVAL, "chunk_tokens %d spans more than %d pages", chunk_tokens, pkd::kMaxCtaPages);
         pl.chunk = chunk_tokens;
     } else {
-        int splits = (kTargetCtas + units - 1) / units;
+        const int target = pl.mma && pl.mt == 2 ? kTargetCtasPair : kTargetCtas;
+        int splits = (target + units - 1) / units;
         const int by_len = (pl.max_vis + kMaxChunk - 1) / kMaxChunk;
         if (by_len > splits) splits = by_len;
         if (splits < 1) splits = 1;

@@ -199,7 +199,9 @@ __device__ __forceinline__ void zero_tail_v(uint8_t* stage_gen, int nvalid, int 
 // memory.  Merge the warps; then either write the result (one chunk) or
 // publish the chunk's (normalised output, LSE) and let the last chunk's CTA
 // merge all chunks by LSE.
-template <int D, int OSTRIDE>
+// NS: number of per-warp (or per-warp-pair) states to merge, state k at
+// rows k*mrows of wm, wl and O.
+template <int D, int OSTRIDE, int NS = kNW>
 __device__ void cta_finish(const DecodeParams& p, const CtaWork& w, const float* O, const float* wm,
                            const float* wl, int mrows, int* flag) {
     const int M = p.M;
@@ -212,11 +214,11 @@ __device__ void cta_finish(const DecodeParams& p, const CtaWork& w, const float*
         const int r = e / D, d = e % D;
         float mx = -INFINITY;
 #pragma unroll
-        for (int k = 0; k < kNW; ++k) mx = fmaxf(mx, wm[k * mrows + r]);
+        for (int k = 0; k < NS; ++k) mx = fmaxf(mx, wm[k * mrows + r]);
         float lsum = 0.f, o = 0.f;
         if (mx != -INFINITY) {
 #pragma unroll
-            for (int k = 0; k < kNW; ++k) {
+            for (int k = 0; k < NS; ++k) {
                 const float s = fast_exp2(wm[k * mrows + r] - mx);
                 lsum += wl[k * mrows + r] * s;
                 o += O[(k * mrows + r) * OSTRIDE + d] * s;

@@ -136,4 +136,146 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p
     cta_finish<D, S::OSTRIDE>(p, w, O, wm, wl, S::MROWS, flag);
 }
 
+// Query blocks of 17..32 rows (M = sq * Hq/Hkv).  One warp holding both
+// 16-row tiles needs two CTAs' worth of registers per SM and twice the tensor
+// work per stage; instead the four warps form two pairs.  The warps of a pair
+// hold rows [0, 16) and [16, 32) and consume the same stages from one shared
+// ring (pair p takes stages p, p + 2, ...), so every stage is loaded once and
+// each warp does half the tensor work.  A buffer is refilled once both warps
+// of its pair have arrived on its "empty" barrier (count 2); the pair's first
+// warp issues the copies.  The pairs' states are merged like the warps' of
+// the one-warp kernel.
+template <int D, int NBUF>
+struct PairShape {
+    static constexpr int KBOX = D * 2 / 128;
+    static constexpr int HALF = KBOX * 2048;
+    static constexpr int STAGE = 2 * HALF;
+    static constexpr int PAIRS = kNW / 2;
+    static constexpr int MROWS = 32;
+    static constexpr int QSTRIDE = D * 2 + 16;
+    static constexpr int OSTRIDE = D + 4;
+    static constexpr int RING = PAIRS * NBUF * STAGE;
+    static constexpr int MERGE = PAIRS * MROWS * OSTRIDE * 4;
+    static constexpr int BIG = RING > MERGE ? RING : MERGE;
+    static constexpr int OFF_BARS = BIG;                        // full[PAIRS][NBUF], then empty[PAIRS][NBUF]
+    static constexpr int OFF_PAGES = OFF_BARS + 2 * PAIRS * NBUF * 8;
+    static constexpr int OFF_Q = 0;                             // q rows staged in the ring before any copy
+    static constexpr int OFF_ML = OFF_PAGES + kMaxCtaPages * 4;
+    static constexpr int OFF_FLAG = OFF_ML + 2 * PAIRS * MROWS * 4;
+    static constexpr int SMEM = OFF_FLAG + 16 + 1024;           // three CTAs per SM
+    static_assert(MROWS * QSTRIDE <= RING, "q rows fit the ring");
+};
+
+template <int D, bool kBF16, int NBUF>
+__global__ void __launch_bounds__(kNW * 32, 3)  // three CTAs per SM fit the shared memory
+decode_mma_pair_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p) {
+    using S = PairShape<D, NBUF>;
+    using W = MmaWarp<D, kBF16, 1, 2>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::OFF_BARS);
+    int* pages = reinterpret_cast<int*>(smem + S::OFF_PAGES);
+    uint8_t* qs = smem + S::OFF_Q;
+    float* wm = reinterpret_cast<float*>(smem + S::OFF_ML);
+    float* wl = wm + S::PAIRS * S::MROWS;
+    int* flag = reinterpret_cast<int*>(smem + S::OFF_FLAG);
+
+    CtaWork w;
+    if (!cta_setup<D>(p, w)) return;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int pair = warp >> 1, half = warp & 1;
+    if (tid == 0) {
+        prefetch_tmap(&tmap);
+        for (int i = 0; i < S::PAIRS * NBUF; ++i) {
+            mbar_init(smem_u32(bars + i), 1);                         // full: the copy's bytes
+            mbar_init(smem_u32(bars + S::PAIRS * NBUF + i), 2);       // empty: both warps of the pair
+        }
+        fence_barrier_init();
+    }
+    load_cta_pages(p, w, pages);
+    {
+        constexpr int VPR = D * 2 / 16;
+        const uint4* qg = reinterpret_cast<const uint4*>(p.q);
+        for (int e = tid; e < S::MROWS * VPR; e += blockDim.x) {
+            const int r = e / VPR, v = e % VPR;
+            uint4 val = make_uint4(0u, 0u, 0u, 0u);
+            if (r < p.M) {
+                const int i = r / p.G, g = r % p.G;
+                const long long row = (static_cast<long long>(w.b) * p.sq + i) * p.Hq + w.hk * p.G + g;
+                val = __ldg(qg + row * VPR + v);
+            }
+            *reinterpret_cast<uint4*>(qs + r * S::QSTRIDE + v * 16) = val;
+        }
+    }
+    __syncthreads();
+
+    const int nst = (w.t1 - w.t0 + kStageTok - 1) / kStageTok;
+    const int my_n = nst > pair ? (nst - pair + S::PAIRS - 1) / S::PAIRS : 0;
+    uint8_t* ring_gen = smem + pair * NBUF * S::STAGE;
+    const uint32_t ring = smem_u32(ring_gen);
+    const uint32_t full0 = smem_u32(bars + pair * NBUF);
+    const uint32_t empty0 = smem_u32(bars + S::PAIRS * NBUF + pair * NBUF);
+    const bool producer = half == 0 && lane == 0;
+    const uint64_t pol = policy_evict_first();
+
+    W wp;
+    wp.row0 = half * 16;
+    wp.load_q(smem_u32(qs) + half * 16 * S::QSTRIDE, S::QSTRIDE, lane);  // into registers
+    wp.reset();
+    fence_proxy_async();  // the q rows were written (generic proxy) where the copies land
+    __syncthreads();      // every warp has its q fragments: the ring may be filled
+    if (producer) {
+        for (int k = 0; k < NBUF && k < my_n; ++k)
+            issue_stage<D, 2>(&tmap, p, w, pages, pair + k * S::PAIRS, ring + k * S::STAGE, full0 + 8 * k, pol);
+    }
+    const int L = w.L, row0 = half * 16;
+
+    int timed_out = 0, consumed = 0;
+    for (int k = 0; k < my_n; ++k) {
+        const int buf = k % NBUF;
+        const uint32_t parity = (k / NBUF) & 1;
+        if (!mbar_wait(full0 + 8 * buf, parity, p.status)) {
+            timed_out = 1;
+            break;
+        }
+        consumed = k + 1;
+        const int tok0 = w.t0 + (pair + k * S::PAIRS) * kStageTok;
+        int nvalid = min(kStageTok, w.t1 - tok0);
+        if (pages[(tok0 - w.t0) / p.P] < 0) nvalid = 0;
+        const uint32_t st = ring + buf * S::STAGE;
+        // both warps zero the same tail rows (the same zeros: benign)
+        if (nvalid < kStageTok) zero_tail_v<D, 2>(ring_gen + buf * S::STAGE, nvalid, lane);
+        wp.consume(st, S::HALF, nvalid, nvalid < kStageTok || p.causal, p.scale_log2, 0.f,
+                   [&](int row, int kt) { return row_sees(p, L, row0 + row, tok0 + kt); }, lane);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * buf);
+        if (producer && k + NBUF < my_n) {
+            // both warps are done with this buffer: refill it
+            if (!mbar_wait(empty0 + 8 * buf, parity, p.status)) {
+                timed_out = 1;
+            } else {
+                fence_proxy_async();
+                issue_stage<D, 2>(&tmap, p, w, pages, pair + (k + NBUF) * S::PAIRS, st, full0 + 8 * buf, pol);
+            }
+        }
+        if (__shfl_sync(kFull, timed_out, 0)) break;
+    }
+    if (timed_out) {
+        // let this pair's other copies land before the CTA leaves or reuses the ring
+        if (lane == 0) raise_status(p, kErrTimeout);
+        for (int k = consumed; k < my_n && k < consumed + NBUF; ++k)
+            mbar_wait(full0 + 8 * (k % NBUF), (k / NBUF) & 1, p.status);
+    }
+
+    // ---- per-pair states to shared memory (the ring is reused for O)
+    wp.reduce_l();
+    __syncthreads();
+    float* O = reinterpret_cast<float*>(smem);
+    wp.store(O + (pair * S::MROWS + row0) * S::OSTRIDE, wm + pair * S::MROWS + row0, wl + pair * S::MROWS + row0,
+             S::OSTRIDE, lane);
+    __syncthreads();
+    cta_finish<D, S::OSTRIDE, S::PAIRS>(p, w, O, wm, wl, S::MROWS, flag);
+}
+
 }  // namespace pkd
