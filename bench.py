@@ -77,12 +77,17 @@ def load_peaks() -> dict:
     return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
 
 
+# sources that build neither the paged-decode kernels nor their launch plan
+NON_DECODE_SOURCES = ("segment.cu", "segment.cuh", "cache_write.cu", "static_ws.cu")
+
+
 def source_digest() -> str:
-    """sha256 over the kernel sources: a traffic figure is valid only for this digest."""
+    """sha256 over the paged-decode kernel sources and their launch plan: a
+    traffic figure is valid only for this digest."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_decode_15_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
+        if name.endswith((".cu", ".cuh", ".h")) and name not in NON_DECODE_SOURCES:
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
