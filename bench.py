@@ -172,6 +172,7 @@ class PagedRunner:
         self.max_kv_len = int(case.block_table.shape[1] * case.page_size)
         kv_code = {"bf16": pkd.BF16, "fp16": pkd.FP16, "fp8": pkd.FP8_E4M3}[case.dtype]
         self.chunk, self.path, self.grid, self.flat = args.chunk, args.path, args.grid, args.flat
+        self.balanced = args.balanced
         flags = paged_flags(case, args, pkd)
         self.ws = torch.empty(pkd.workspace_size(case.batch, case.sq, case.num_heads, case.num_kv_heads,
                                                  case.head_dim, case.page_size, self.max_kv_len, kv_code, case.window,
@@ -186,7 +187,8 @@ class PagedRunner:
         self.pkd.paged_decode(self.q, self.cache, self.bt, self.lens, c.scale, c.window, out=self.out, lse=self.lse,
                               q_scale=c.q_scale, k_scale=c.k_scale, v_scale=c.v_scale, max_kv_len=self.max_kv_len,
                               workspace=self.ws, causal=c.causal, chunk_tokens=self.chunk,
-                              force_fma=self.path == "fma", grid=self.grid, flat=self.flat)
+                              force_fma=self.path == "fma", grid=self.grid, flat=self.flat,
+                              balanced=self.balanced)
 
     def check(self):
         if self.pkd.workspace_check(self.ws) != self.pkd.OK:
@@ -468,7 +470,8 @@ def workload_config(case, args) -> dict:
 
 def paged_flags(case, args, pkd) -> int:
     return (pkd.FLAG_CAUSAL if case.causal else 0) | (pkd.FLAG_FMA if args.path == "fma" else 0) | \
-        (pkd.FLAG_GRID if args.grid else 0) | (pkd.FLAG_FLAT if args.flat else 0)
+        (pkd.FLAG_GRID if args.grid else 0) | (pkd.FLAG_FLAT if args.flat else 0) | \
+        (pkd.FLAG_BALANCED if args.balanced else 0)
 
 
 def paged_kernel_name(case, args) -> str:
@@ -502,6 +505,7 @@ def main():
                     help="library default (tensor cores for 16-bit caches) or CUDA cores")
     ap.add_argument("--grid", action="store_true", help="force the chunked grid (one CTA per Split-KV chunk)")
     ap.add_argument("--flat", action="store_true", help="force the persistent flat partition")
+    ap.add_argument("--balanced", action="store_true", help="force the persistent per-CTA partition")
     ap.add_argument("--l2-flush", default="write-read", choices=["write", "write-read"],
                     help="how L2 is evicted before every timed step: a 512 MiB write (it leaves up to an L2 of "
                          "dirty lines whose write-back lands inside the timed step), or that write followed by a "

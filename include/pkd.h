@@ -49,6 +49,7 @@ typedef enum {
 #define PKD_FLAG_FMA 4u         /* CUDA cores instead (only when sq*Hq/Hkv <= 8; always for fp8) */
 #define PKD_FLAG_GRID 8u        /* one CTA per Split-KV chunk instead of the persistent flat partition */
 #define PKD_FLAG_FLAT 16u       /* the persistent flat partition whatever the shapes (batch <= 1024) */
+#define PKD_FLAG_BALANCED 32u   /* the persistent per-CTA partition (16-bit caches, tensor cores) */
 
 /* Library version, major*10000 + minor*100 + patch. */
 int pkd_version(void);

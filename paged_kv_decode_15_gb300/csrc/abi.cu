@@ -50,7 +50,8 @@ constexpr size_t kHeader = 256;    // workspace status word lives in the first b
 
 struct Plan {
     bool mma;
-    bool flat;
+    bool flat;     // persistent per-warp partition
+    bool bal;      // persistent per-CTA partition
     int M, G;
     int mt, nt;    // tensor-core tiles
     int lpt, mr;   // CUDA-core lanes per key, padded rows
@@ -79,9 +80,15 @@ pkd_status make_plan(int B, int sq, int Hq, int Hkv, int D, int P, int max_kv_le
     // faster (gqa_decode_b64: 108.6 vs 126.9 us).  PKD_FLAG_GRID forces the grid.
     const bool many_units = (long long)B * Hkv >= 256;
     const bool flat_only = kv == PKD_FP8_E4M3 || (long long)sq * (Hq / Hkv) > 16;
-    if ((flags & PKD_FLAG_GRID) && (flags & PKD_FLAG_FLAT))
-        return fail(PKD_EINVAL, "PKD_FLAG_GRID and PKD_FLAG_FLAT exclude each other");
-    pl.flat = B <= pkd::kFlatMaxBatch && !(flags & PKD_FLAG_GRID) &&
+    if (((flags & PKD_FLAG_GRID) != 0) + ((flags & PKD_FLAG_FLAT) != 0) + ((flags & PKD_FLAG_BALANCED) != 0) > 1)
+        return fail(PKD_EINVAL, "PKD_FLAG_GRID, PKD_FLAG_FLAT and PKD_FLAG_BALANCED exclude each other");
+    pl.bal = false;
+    if (flags & PKD_FLAG_BALANCED) {
+        if (kv == PKD_FP8_E4M3 || (flags & PKD_FLAG_FMA))
+            return fail(PKD_EUNSUPPORTED, "the per-CTA partition runs 16-bit caches on tensor cores only");
+        pl.bal = true;
+    }
+    pl.flat = !pl.bal && B <= pkd::kFlatMaxBatch && !(flags & PKD_FLAG_GRID) &&
               ((flags & PKD_FLAG_FLAT) || flat_only || !many_units);
     if (kv == PKD_FP8_E4M3 && (!pl.flat || (flags & PKD_FLAG_FMA))) {
         // the chunked grid reads fp8 on CUDA cores only
@@ -131,7 +138,9 @@ pkd_status make_plan(int B, int sq, int Hq, int Hkv, int D, int P, int max_kv_le
     pl.off_lse = pl.off_counters + round_up((size_t)units * 4, 256);
     // partial results: per (unit, chunk) for the chunked grid, per (warp, side)
     // for the flat partition
-    const size_t parts = pl.flat ? (size_t)pkd::kFlatMaxWorkers * 2 : (size_t)units * pl.max_splits;
+    const size_t parts = pl.flat  ? (size_t)pkd::kFlatMaxWorkers * 2
+                         : pl.bal ? (size_t)pkd::kFlatMaxWorkers / pkd::kNW * 2  // two per CTA, <= 512 CTAs
+                                  : (size_t)units * pl.max_splits;
     pl.off_out = pl.off_lse + round_up(parts * M * 4, 256);
     pl.bytes = pl.off_out + round_up(parts * M * D * 4, 256);
     return PKD_OK;
@@ -293,6 +302,7 @@ const char* pkd_paged_decode_kernel_name(int batch, int sq, int num_heads, int n
     if (make_plan(batch, sq, num_heads, num_kv_heads, head_dim, page_size, max_kv_len, kv_dtype, window,
                   chunk_tokens, flags, pl) != PKD_OK)
         return nullptr;
+    if (pl.bal) return "persistent per-CTA partition, tensor cores";
     if (pl.flat) return pl.mma ? "persistent flat partition, tensor cores" : "persistent flat partition, CUDA cores";
     return pl.mma ? "chunked grid, tensor cores" : "chunked grid, CUDA cores";
 }
@@ -390,7 +400,9 @@ pkd_status pkd_paged_decode(const void* q, pkd_dtype q_dtype, const void* kv_cac
     cudaError_t e;
     cudaStream_t s = (cudaStream_t)stream;
     const int max_ctas = pkd::kFlatMaxWorkers / pkd::kNW;
-    if (pl.flat && pl.mma)
+    if (pl.bal)
+        e = pkd::launch_decode_bal(head_dim, kv_dtype == PKD_BF16, pl.mt, pl.nt, tmap, p, s);
+    else if (pl.flat && pl.mma)
         e = kv_dtype == PKD_BF16   ? pkd::launch_flat_mma_bf16(head_dim, pl.mt, pl.nt, tmap, p, max_ctas, s)
             : kv_dtype == PKD_FP16 ? pkd::launch_flat_mma_fp16(head_dim, pl.mt, pl.nt, tmap, p, max_ctas, s)
                                    : pkd::launch_flat_mma_fp8(head_dim, pl.mt, pl.nt, tmap, p, max_ctas, s);

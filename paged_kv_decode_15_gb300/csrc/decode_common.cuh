@@ -72,6 +72,39 @@ __device__ __forceinline__ long long out_index(const DecodeParams& p, int b, int
     return ((static_cast<long long>(b) * p.sq + i) * p.Hq + hk * p.G + g) * D + d;
 }
 
+// Sequence length of request b, clamped to [0, max_kv_len]; an out-of-range
+// length raises the status word when `report` is set.
+__device__ __forceinline__ int clamp_len(const DecodeParams& p, int b, bool report) {
+    int L = p.seq_lens[b];
+    if (L < 0 || L > p.max_kv_len) {
+        if (report) raise_status(p, kErrBounds);
+        L = L < 0 ? 0 : p.max_kv_len;
+    }
+    return L;
+}
+
+// First visible key of a request of length L: 0, or with a window the
+// page-aligned start shared by the query block (dense), or the earliest key
+// any row of the block can see, page-aligned (causal).
+__device__ __forceinline__ int visible_lo(const DecodeParams& p, int L) {
+    if (p.window <= 0) return 0;
+    const int first = p.causal ? L - p.sq - p.window + 1 : L - (p.window + p.sq - 1);
+    return first > 0 ? (first / p.P) * p.P : 0;
+}
+
+// out = 0, lse = -inf for every row of request b (it has no visible key).
+template <int D>
+__device__ __forceinline__ void write_empty_request(const DecodeParams& p, int b) {
+    for (int e = threadIdx.x; e < p.Hkv * p.M * D; e += blockDim.x) {
+        const int hk = e / (p.M * D), r = (e / D) % p.M, d = e % D;
+        store_out(p.out, out_index(p, b, hk, r, d, D), 0.f, p.out_dtype);
+        if (d == 0 && p.lse) {
+            const int i = r / p.G, g = r % p.G;
+            p.lse[(static_cast<long long>(b) * p.sq + i) * p.Hq + hk * p.G + g] = -INFINITY;
+        }
+    }
+}
+
 // Visible-key range and Split-KV chunk of this CTA.  Returns false when the
 // CTA has nothing to do (it has then written what it owed).
 template <int D>
@@ -127,10 +160,12 @@ __device__ __forceinline__ bool row_sees(const DecodeParams& p, int L, int row, 
     return p.window <= 0 || tok >= pos - (p.window - 1);
 }
 
-// Load the page indices of this CTA's keys into shared memory; a page outside
-// [0, num_pages) becomes -1 (its keys are skipped) and raises the status word.
+// Load the page indices of this CTA's keys [t0, t1) into shared memory
+// (pages[i] holds table column t0/P + i; t0 need not be page-aligned); a page
+// outside [0, num_pages) becomes -1 (its keys are skipped) and raises the
+// status word.
 __device__ __forceinline__ void load_cta_pages(const DecodeParams& p, const CtaWork& w, int* pages) {
-    const int npages = (w.t1 - w.t0 + p.P - 1) / p.P;
+    const int npages = w.t1 > w.t0 ? (w.t1 - 1) / p.P - w.t0 / p.P + 1 : 0;
     const long long base = static_cast<long long>(w.b) * p.bt_stride + w.t0 / p.P;
     for (int i = threadIdx.x; i < npages; i += blockDim.x) {
         int pg = p.block_table[base + i];
@@ -140,6 +175,11 @@ __device__ __forceinline__ void load_cta_pages(const DecodeParams& p, const CtaW
         }
         pages[i] = pg;
     }
+}
+
+// Page of key `tok` (in [t0, t1)) from the list load_cta_pages made.
+__device__ __forceinline__ int page_of(const DecodeParams& p, const CtaWork& w, const int* pages, int tok) {
+    return pages[tok / p.P - w.t0 / p.P];
 }
 
 // Issue the TMA load of one 16-key stage.  The stage map views the cache as
@@ -154,7 +194,7 @@ __device__ __forceinline__ void issue_stage(const CUtensorMap* tmap, const Decod
     constexpr int KBOX = ROWB / 128;  // 128-byte boxes per half
     constexpr int HALF = KBOX * 2048;
     const int tok = w.t0 + stage * kStageTok;
-    const int pg = pages[(tok - w.t0) / p.P];
+    const int pg = page_of(p, w, pages, tok);
     if (pg < 0) {
         mbar_arrive(bar);
         return;
@@ -170,7 +210,7 @@ __device__ __forceinline__ void prefetch_stage(const CUtensorMap* tmap, const De
                                                const int* pages, int stage) {
     const int tok = w.t0 + stage * kStageTok;
     if (tok >= w.t1) return;
-    const int pg = pages[(tok - w.t0) / p.P];
+    const int pg = page_of(p, w, pages, tok);
     if (pg < 0) return;
     tma_prefetch_3d(tmap, 0, (pg * p.Hkv + w.hk) * p.P + (tok % p.P), 0);
 }
@@ -201,14 +241,17 @@ __device__ __forceinline__ void zero_tail_v(uint8_t* stage_gen, int nvalid, int 
 // merge all chunks by LSE.
 // NS: number of per-warp (or per-warp-pair) states to merge, state k at
 // rows k*mrows of wm, wl and O.
-template <int D, int OSTRIDE, int NS = kNW>
-__device__ void cta_finish(const DecodeParams& p, const CtaWork& w, const float* O, const float* wm,
-                           const float* wl, int mrows, int* flag) {
+// part_of(j) is the workspace slot of split j of the unit (this CTA's split
+// is w.split): [M] LSEs at part_lse + slot*M, [M, D] outputs at part_out +
+// slot*M*D.
+template <int D, int OSTRIDE, int NS, class PartOf>
+__device__ void cta_finish_parts(const DecodeParams& p, const CtaWork& w, const float* O, const float* wm,
+                                 const float* wl, int mrows, int* flag, PartOf part_of) {
     const int M = p.M;
     const int unit = w.b * p.Hkv + w.hk;
     const bool single = w.nsplit == 1;
-    float* pout = p.part_out + (static_cast<long long>(unit) * p.max_splits + w.split) * M * D;
-    float* plse = p.part_lse + (static_cast<long long>(unit) * p.max_splits + w.split) * M;
+    float* pout = p.part_out + static_cast<long long>(part_of(w.split)) * M * D;
+    float* plse = p.part_lse + static_cast<long long>(part_of(w.split)) * M;
 
     for (int e = threadIdx.x; e < M * D; e += blockDim.x) {
         const int r = e / D, d = e % D;
@@ -251,20 +294,19 @@ __device__ void cta_finish(const DecodeParams& p, const CtaWork& w, const float*
     __syncthreads();
     if (!*flag) return;
     __threadfence();
-    const float* uout = p.part_out + static_cast<long long>(unit) * p.max_splits * M * D;
-    const float* ulse = p.part_lse + static_cast<long long>(unit) * p.max_splits * M;
     for (int e = threadIdx.x; e < M * D; e += blockDim.x) {
         const int r = e / D, d = e % D;
         float mx = -INFINITY;
-        for (int c = 0; c < w.nsplit; ++c) mx = fmaxf(mx, __ldcg(ulse + c * M + r));
+        for (int c = 0; c < w.nsplit; ++c) mx = fmaxf(mx, __ldcg(p.part_lse + static_cast<long long>(part_of(c)) * M + r));
         float wsum = 0.f, o = 0.f;
         if (mx != -INFINITY) {
             for (int c = 0; c < w.nsplit; ++c) {
-                const float lc = __ldcg(ulse + c * M + r);
+                const long long slot = part_of(c);
+                const float lc = __ldcg(p.part_lse + slot * M + r);
                 if (lc == -INFINITY) continue;  // an empty chunk is never read
                 const float s = fast_exp2(lc - mx);
                 wsum += s;
-                o += s * __ldcg(uout + (static_cast<long long>(c) * M + r) * D + d);
+                o += s * __ldcg(p.part_out + (slot * M + r) * D + d);
             }
         }
         const float on = wsum > 0.f ? o / wsum : 0.f;
@@ -275,6 +317,15 @@ __device__ void cta_finish(const DecodeParams& p, const CtaWork& w, const float*
                 wsum > 0.f ? (mx + __log2f(wsum)) * kLn2 : -INFINITY;
         }
     }
+}
+
+// The chunked grid: split j of unit u has slot u * max_splits + j.
+template <int D, int OSTRIDE, int NS = kNW>
+__device__ void cta_finish(const DecodeParams& p, const CtaWork& w, const float* O, const float* wm,
+                           const float* wl, int mrows, int* flag) {
+    const long long unit = static_cast<long long>(w.b) * p.Hkv + w.hk;
+    cta_finish_parts<D, OSTRIDE, NS>(p, w, O, wm, wl, mrows, flag,
+                                     [&](int j) { return unit * p.max_splits + j; });
 }
 
 }  // namespace pkd

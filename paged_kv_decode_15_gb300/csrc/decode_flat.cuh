@@ -39,13 +39,6 @@ struct FlatShape {
     static constexpr int SMEM = OFF_MERGE + kNW * 3 * 32 * 4 + 1024;
 };
 
-// First visible key of a request of length L (page-aligned, as cta_setup).
-__device__ __forceinline__ int visible_lo(const DecodeParams& p, int L) {
-    if (p.window <= 0) return 0;
-    const int first = p.causal ? L - p.sq - p.window + 1 : L - (p.window + p.sq - 1);
-    return first > 0 ? (first / p.P) * p.P : 0;
-}
-
 struct StageMeta {
     int b, hk, s, page;
 };

@@ -85,7 +85,7 @@ decode_fma_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p
         const int stage = warp + k * kNW;
         const int tok0 = w.t0 + stage * kStageTok;
         int nvalid = min(kStageTok, w.t1 - tok0);
-        if (pages[(tok0 - w.t0) / p.P] < 0) nvalid = 0;
+        if (page_of(p, w, pages, tok0) < 0) nvalid = 0;
         uint8_t* st = ring_gen + buf * S::STAGE;
         if (nvalid < kStageTok) zero_tail_v<D, ELT>(st, nvalid, lane);
         wp.consume(st, nvalid, [&](int row, int kt) { return row_sees(p, L, row, tok0 + kt); }, lane);

@@ -108,7 +108,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p
         const int stage = warp + k * kNW;
         const int tok0 = w.t0 + stage * kStageTok;
         int nvalid = min(kStageTok, w.t1 - tok0);
-        if (pages[(tok0 - w.t0) / p.P] < 0) nvalid = 0;
+        if (page_of(p, w, pages, tok0) < 0) nvalid = 0;
         const uint32_t st = ring + buf * S::STAGE;
         if (nvalid < kStageTok) zero_tail_v<D, 2>(ring_gen + buf * S::STAGE, nvalid, lane);
         wp.consume(st, S::HALF, nvalid, nvalid < kStageTok || p.causal, p.scale_log2, 0.f,
@@ -242,7 +242,7 @@ decode_mma_pair_kernel(const __grid_constant__ CUtensorMap tmap, const DecodePar
         consumed = k + 1;
         const int tok0 = w.t0 + (pair + k * S::PAIRS) * kStageTok;
         int nvalid = min(kStageTok, w.t1 - tok0);
-        if (pages[(tok0 - w.t0) / p.P] < 0) nvalid = 0;
+        if (page_of(p, w, pages, tok0) < 0) nvalid = 0;
         const uint32_t st = ring + buf * S::STAGE;
         // both warps zero the same tail rows (the same zeros: benign)
         if (nvalid < kStageTok) zero_tail_v<D, 2>(ring_gen + buf * S::STAGE, nvalid, lane);

@@ -21,6 +21,11 @@ cudaError_t launch_decode_mma(int D, bool bf16, int MT, int NT, const CUtensorMa
 cudaError_t launch_decode_fma(int D, int kvt, int LPT, int MR, const CUtensorMap& tmap,
                               const DecodeParams& p, dim3 grid, cudaStream_t stream);
 
+// Persistent per-CTA partition, tensor cores, 16-bit caches: the grid fills
+// the GPU once (at most 512 CTAs, two partial slots each in the workspace).
+cudaError_t launch_decode_bal(int D, bool bf16, int MT, int NT, const CUtensorMap& tmap, const DecodeParams& p,
+                              cudaStream_t stream);
+
 // Persistent flat-partition decode: the grid fills the GPU once (at most
 // max_ctas CTAs, one partial slot pair per warp in the workspace).
 cudaError_t launch_flat_mma_bf16(int D, int MT, int NT, const CUtensorMap& tmap, const DecodeParams& p,

@@ -162,6 +162,17 @@ segmented_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         for (int g = warp; g < groups; g += kNW) my_n += pre[g + 1] - pre[g];
     }
 
+    // Contiguous segments: the last stage of a segment longer than one stage
+    // whose length is not a multiple of 16 is moved back to end at the
+    // segment's last used row; its first rows (read again, from L2) are masked
+    // as already consumed.  No row past the used prefix is then read from
+    // DRAM.  A segment shorter than a stage reads one stage from its start.
+    auto shifted = [&](int g, int sidx) {
+        const int u = su[g];
+        return !kPaged && u > kStageTok && (u % kStageTok) != 0 && sidx == (u - 1) / kStageTok;
+    };
+    auto stage_row = [&](int g, int sidx) { return shifted(g, sidx) ? su[g] - kStageTok : sidx * kStageTok; };
+
     uint8_t* ring_gen = smem + warp * kSegNbuf * S::STAGE;
     const uint32_t ring = smem_u32(ring_gen);
     const uint32_t bar0 = smem_u32(bars + warp * kSegNbuf);
@@ -184,7 +195,7 @@ segmented_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             return;
         }
         const long long row = row_base + (g < p.topk ? static_cast<long long>(g) * p.bs : static_cast<long long>(p.topk) * p.bs) +
-                              static_cast<long long>(sidx) * kStageTok;
+                              stage_row(g, sidx);
         mbar_arrive_expect_tx(bar, S::STAGE);
 #pragma unroll
         for (int bx = 0; bx < D * 2 / 128; ++bx) {
@@ -254,6 +265,9 @@ segmented_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             nvalid = min(kStageTok, ss[g] + su[g] - tok0);
             lo = ss[g] - tok0;
             if (spage[pre[g] + sidx] < 0) nvalid = 0;
+        } else if (shifted(g, sidx)) {
+            nvalid = kStageTok;
+            lo = sidx * kStageTok - stage_row(g, sidx);  // rows the previous stage already took
         } else {
             nvalid = min(kStageTok, su[g] - sidx * kStageTok);
         }

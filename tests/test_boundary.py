@@ -153,3 +153,11 @@ def test_kernel_name_follows_the_plan(lib):
         pkd.kernel_name(2, 1, 8, 2, 96, 16, 100, pkd.BF16)
     with pytest.raises(pkd.PkdError, match="exclude"):
         pkd.kernel_name(*args, pkd.BF16, flags=pkd.FLAG_FLAT | pkd.FLAG_GRID)
+    assert pkd.kernel_name(*args, pkd.BF16, flags=pkd.FLAG_BALANCED) == "persistent per-CTA partition, tensor cores"
+    with pytest.raises(pkd.PkdError, match="16-bit"):
+        pkd.kernel_name(*args, pkd.FP8_E4M3, flags=pkd.FLAG_BALANCED)
+    # the per-CTA partition: two partial slots per CTA (<= 512 CTAs), whatever the lengths or the batch
+    b1 = pkd.workspace_size(64, 1, 32, 8, 128, 16, 4096, pkd.BF16, flags=pkd.FLAG_BALANCED)
+    b2 = pkd.workspace_size(64, 1, 32, 8, 128, 16, 131072, pkd.BF16, flags=pkd.FLAG_BALANCED)
+    assert b1 == b2 and b1 >= 512 * 2 * 4 * 128 * 4
+    assert pkd.kernel_name(4096, 8, 32, 8, 128, 16, 4096, pkd.BF16, flags=pkd.FLAG_BALANCED).startswith("persistent")

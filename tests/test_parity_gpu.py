@@ -69,8 +69,8 @@ SMALL = {
 }
 
 # kernel variants: persistent flat partition / one CTA per chunk; tensor / CUDA cores
-VARIANTS = {"flat": dict(), "grid": dict(grid=True), "flat_fma": dict(force_fma=True),
-            "grid_fma": dict(grid=True, force_fma=True)}
+VARIANTS = {"auto": dict(), "flat": dict(flat=True), "grid": dict(grid=True), "balanced": dict(balanced=True),
+            "flat_fma": dict(force_fma=True), "grid_fma": dict(grid=True, force_fma=True)}
 
 
 def _m(ckw):
@@ -84,6 +84,8 @@ def test_small_cases_match_oracle(name, variant):
     vkw = VARIANTS[variant]
     if (vkw.get("force_fma") or (vkw.get("grid") and ckw.get("dtype") == "fp8")) and _m(ckw) > 8:
         pytest.skip("the CUDA-core kernel takes M <= 8 (fp8 in the chunked grid always runs on it)")
+    if vkw.get("balanced") and ckw.get("dtype") == "fp8":
+        pytest.skip("the per-CTA partition runs 16-bit caches only")
     case = wl.paged_case(name=name, seed=zlib.crc32(name.encode()) % 1000, **ckw)
     _check(case, **kw, **vkw)
 
@@ -215,19 +217,29 @@ def test_gqa_decode_b64_full():
     _check(case)
 
 
-@pytest.mark.parametrize("variant", ["grid", "flat_fma"])
+@pytest.mark.parametrize("variant", ["flat", "balanced", "flat_fma"])
 def test_gqa_decode_b64_other_variants(variant):
     case = wl.gqa_decode_b64()
     _check(case, **VARIANTS[variant])
 
 
+@pytest.mark.parametrize("variant", ["auto", "grid", "balanced"])
 @pytest.mark.parametrize("window", [0, 4096])
-def test_query_block_sq8_sampled(window):
+def test_query_block_sq8_sampled(window, variant):
     case = wl.query_block_sq8(window=window)
-    _check(case, batch_index=[0, 5, 11, 17, 23, 31])
+    _check(case, batch_index=[0, 5, 11, 17, 23, 31], **VARIANTS[variant])
 
 
 @pytest.mark.parametrize("variant", ["flat", "flat_fma"])
 def test_fp8_long_b8_sampled(variant):
     case = wl.fp8_long_b8()
     _check(case, batch_index=[0, 7], **VARIANTS[variant])
+
+
+@pytest.mark.parametrize("sq", [1, 8])
+def test_long_slices_reload_the_page_list(sq):
+    """One 2M-key request on the per-CTA partition: every CTA streams more keys
+    than its page list holds at once, so it reloads the list inside the unit."""
+    case = wl.paged_case(name="long", seq_lens=[2_000_000], sq=sq, num_heads=4, num_kv_heads=1, head_dim=64,
+                         pool_factor=1.0, seed=31 + sq)
+    _check(case, balanced=True)
