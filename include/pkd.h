@@ -154,9 +154,9 @@ pkd_status pkd_paged_decode(const void* q, pkd_dtype q_dtype,
 /*
  * pkd_paged_decode without a caller workspace.  The pages have no counterpart
  * of this call: it exists for callers that cannot allocate device memory at
- * the point where they run decode -- code running while a CUDA graph is being
- * captured (allocation is not a capturable operation), plug-ins whose host
- * runtime owns all device memory, or C callers with no device allocator of
+ * the point where they run decode -- plug-ins whose host runtime owns all
+ * device memory and hands none out, serving loops that must not allocate once
+ * their memory budget is fixed, or C callers with no device allocator of
  * their own.
  *
  * It takes the same arguments as pkd_paged_decode minus the workspace and

@@ -2,11 +2,10 @@
 //
 // pkd_paged_decode needs a workspace for its Split-KV partial results, and
 // asks the caller to provide it.  Some callers cannot allocate device memory
-// when they need to run decode: code running while a CUDA graph is being
-// captured (an allocation is not a capturable operation and would break the
-// capture), plug-ins hosted by a runtime that owns all device memory and
-// hands none out, or C callers that link only this library and have no
-// allocator of their own.  pkd_paged_decode_static serves them: it uses the
+// when they need to run decode: plug-ins hosted by a runtime that owns all
+// device memory and hands none out, serving loops that must not allocate once
+// their memory budget is fixed, or C callers that link only this library and
+// have no allocator of their own.  pkd_paged_decode_static serves them: it uses the
 // fixed scratch array below, which is part of the library image, so the call
 // itself allocates nothing.
 #include <cuda_runtime.h>

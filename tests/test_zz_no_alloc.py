@@ -1,7 +1,8 @@
 """pkd_paged_decode_static: paged decode for callers that cannot allocate.
 
-Callers that run decode while a CUDA graph is being captured, or inside a
-runtime that owns all device memory, cannot hand the library a workspace.
+Callers inside a runtime that owns all device memory, serving loops that
+must not allocate once their memory budget is fixed, and C callers without
+an allocator cannot hand the library a workspace.
 The static entry point uses a scratch array compiled into the library
 instead.  This checks it through the C ABI against pkd_paged_decode (with a
 caller workspace) on two calls in a row, the second with different lengths,
