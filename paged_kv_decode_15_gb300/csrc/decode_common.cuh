@@ -11,9 +11,6 @@ namespace pkd {
 constexpr int kNW = 4;          // consumer warps per CTA (one warp group)
 constexpr int kStageTok = 16;   // keys per pipeline stage (one TMA box height)
 constexpr int kMaxCtaPages = 256;
-// Stages a warp asks L2 to fetch beyond its shared-memory ring (0: none).
-// Measured on gqa_decode_b64: 4 stages cost 14 us per call, so it is off.
-constexpr int kPrefetch = 0;
 constexpr int kFlatMaxBatch = 1024;    // the flat kernel keeps per-request tables in shared memory
 constexpr int kFlatMaxWorkers = 2048;  // and two partial slots per warp in the workspace
 constexpr float kLn2 = 0.69314718055994530942f;
@@ -202,17 +199,6 @@ __device__ __forceinline__ void issue_stage(const CUtensorMap* tmap, const Decod
     const int row = (pg * p.Hkv + w.hk) * p.P + (tok % p.P);
     mbar_arrive_expect_tx(bar, 2 * HALF);
     tma_load_3d(buf, tmap, 0, row, 0, bar, policy);  // the whole 16-key stage in one copy
-}
-
-// L2 prefetch of a stage this CTA will load later (no-op past its keys or
-// for a skipped page).
-__device__ __forceinline__ void prefetch_stage(const CUtensorMap* tmap, const DecodeParams& p, const CtaWork& w,
-                                               const int* pages, int stage) {
-    const int tok = w.t0 + stage * kStageTok;
-    if (tok >= w.t1) return;
-    const int pg = page_of(p, w, pages, tok);
-    if (pg < 0) return;
-    tma_prefetch_3d(tmap, 0, (pg * p.Hkv + w.hk) * p.P + (tok % p.P), 0);
 }
 
 // Zero the V rows [nvalid, 16) of a stage so that masked keys (past the

@@ -238,17 +238,7 @@ decode_flat_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams 
         tma_load_3d(buf, &tmap, 0, row, 0, bar, pol);
     };
 
-    auto prefetch = [&](const StageMeta& m) {  // lane 0 only
-        if (m.b < 0 || m.page < 0) return;
-        const int tok = visible_lo(p, lens[m.b]) + m.s * kStageTok;
-        tma_prefetch_3d(&tmap, 0, (m.page * p.Hkv + m.hk) * p.P + (tok % p.P), 0);
-    };
-
     StageMeta cur = fetch(f0 + lane), nxt = fetch(f0 + 32 + lane);
-    for (int k = NBUF; k < NBUF + kPrefetch; ++k) {
-        const StageMeta m = shfl_meta(cur, k);
-        if (lane == 0 && k < n && rt == 0) prefetch(m);
-    }
     for (int k = 0; k < NBUF && k < n; ++k) {
         const StageMeta m = shfl_meta(cur, k);
         if (lane == 0) issue(k, m);
@@ -342,11 +332,7 @@ decode_flat_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams 
         const int j = k + NBUF;
         if (j < n) {
             const StageMeta mj = shfl_meta((j >> 5) == (k >> 5) ? cur : nxt, j & 31);
-            const int jp = j + kPrefetch;
-            StageMeta mp;
-            if (kPrefetch > 0) mp = shfl_meta((jp >> 5) == (k >> 5) ? cur : nxt, jp & 31);
             if (lane == 0) {
-                if (kPrefetch > 0 && jp < n && rt == 0) prefetch(mp);
                 fence_proxy_async();
                 issue(j, mj);
             }

@@ -62,8 +62,6 @@ decode_fma_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p
     const uint32_t ring = smem_u32(ring_gen);
     const uint32_t bar0 = smem_u32(bars + warp * NBUF);
     const uint64_t pol = policy_evict_first();
-    if (kPrefetch > 0 && lane == 0)
-        for (int k = NBUF; k < NBUF + kPrefetch; ++k) prefetch_stage(&tmap, p, w, pages, warp + k * kNW);
     if (lane == 0)
         for (int k = 0; k < NBUF && k < my_n; ++k)
             issue_stage<D, ELT>(&tmap, p, w, pages, warp + k * kNW, ring + k * S::STAGE, bar0 + 8 * k, pol);
@@ -91,7 +89,6 @@ decode_fma_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p
         wp.consume(st, nvalid, [&](int row, int kt) { return row_sees(p, L, row, tok0 + kt); }, lane);
         __syncwarp();
         if (lane == 0 && k + NBUF < my_n) {
-            if (kPrefetch > 0) prefetch_stage(&tmap, p, w, pages, warp + (k + NBUF + kPrefetch) * kNW);
             fence_proxy_async();
             issue_stage<D, ELT>(&tmap, p, w, pages, warp + (k + NBUF) * kNW, ring + buf * S::STAGE,
                                 bar0 + 8 * buf, pol);

@@ -5,19 +5,20 @@
 namespace pkd {
 
 constexpr int kMmaNbuf = 2;
+constexpr int kGridWarps = 4;  // warps per CTA of the one-tile kernel
 constexpr int kPairNbuf = 4;  // per warp pair: the same 64 KiB of ring per CTA as four rings of two
 
 template <int D, bool kBF16, int MT, int NT>
 static cudaError_t launch_one(const CUtensorMap& tmap, const DecodeParams& p, dim3 grid, cudaStream_t stream) {
-    using S = MmaShape<D, MT, NT, kMmaNbuf>;
-    auto kern = decode_mma_kernel<D, kBF16, MT, NT, kMmaNbuf>;
+    using S = MmaShape<D, MT, NT, kMmaNbuf, kGridWarps>;
+    auto kern = decode_mma_kernel<D, kBF16, MT, NT, kMmaNbuf, kGridWarps>;
     static bool configured = false;  // benign race: the attribute call is idempotent
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    kern<<<grid, kNW * 32, S::SMEM, stream>>>(tmap, p);
+    kern<<<grid, kGridWarps * 32, S::SMEM, stream>>>(tmap, p);
     return cudaGetLastError();
 }
 

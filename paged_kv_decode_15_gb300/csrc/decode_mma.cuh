@@ -18,7 +18,7 @@
 
 namespace pkd {
 
-template <int D, int MT, int NT, int NBUF>
+template <int D, int MT, int NT, int NBUF, int NW = kNW>
 struct MmaShape {
     static constexpr int ELT = 2;
     static constexpr int ROWB = D * ELT;
@@ -28,40 +28,85 @@ struct MmaShape {
     static constexpr int MROWS = MT * 16;
     static constexpr int QSTRIDE = D * 2 + 16;           // bytes per staged q row
     static constexpr int OSTRIDE = D + 4;                // floats per merge row
-    static constexpr int RING = kNW * NBUF * STAGE;
-    static constexpr int MERGE = kNW * MROWS * OSTRIDE * 4;
+    static constexpr int RING = NW * NBUF * STAGE;
+    static constexpr int MERGE = NW * MROWS * OSTRIDE * 4;
     static constexpr int BIG = RING > MERGE ? RING : MERGE;
     static constexpr int OFF_BARS = BIG;
-    static constexpr int OFF_PAGES = OFF_BARS + kNW * NBUF * 8;
+    static constexpr int OFF_PAGES = OFF_BARS + NW * NBUF * 8;
     static constexpr int OFF_Q = OFF_PAGES + kMaxCtaPages * 4;
     static constexpr int OFF_ML = OFF_Q + MROWS * QSTRIDE;
-    static constexpr int OFF_FLAG = OFF_ML + 2 * kNW * MROWS * 4;
+    static constexpr int OFF_FLAG = OFF_ML + 2 * NW * MROWS * 4;
     static constexpr int SMEM = OFF_FLAG + 16 + 1024;    // + slack to align the base to 1 KiB
 };
 
-template <int D, bool kBF16, int MT, int NT, int NBUF>
-__global__ void __launch_bounds__(kNW * 32)
+// Without a window a chunk's first key is split * chunk whatever the
+// request's length, so the chunk's block-table entries can be read while the
+// length itself is read: the page list is then ready one memory round trip
+// earlier.  Entries are validated once the length is known; columns at or
+// past ceil(max_kv_len / P) are never read.
+template <int NTHREADS>
+struct SpecPages {
+    static constexpr int PER = (kMaxCtaPages + NTHREADS - 1) / NTHREADS;
+    int ent[PER];
+    bool on = false;
+    __device__ __forceinline__ void load(const DecodeParams& p) {
+        on = p.window <= 0;
+        if (!on) return;
+        const int b = blockIdx.z, col0 = blockIdx.x * (p.chunk / p.P);
+        const int cols = (p.max_kv_len + p.P - 1) / p.P;
+#pragma unroll
+        for (int j = 0; j < PER; ++j) {
+            const int i = threadIdx.x + j * NTHREADS;
+            ent[j] = (i < p.chunk / p.P && col0 + i < cols)
+                         ? p.block_table[static_cast<long long>(b) * p.bt_stride + col0 + i] : -1;
+        }
+    }
+    // the page list of [w.t0, w.t1) (w.t0 = split * chunk here)
+    __device__ __forceinline__ void store(const DecodeParams& p, const CtaWork& w, int* pages) const {
+        const int npages = (w.t1 - 1) / p.P - w.t0 / p.P + 1;
+#pragma unroll
+        for (int j = 0; j < PER; ++j) {
+            const int i = threadIdx.x + j * NTHREADS;
+            if (i < npages) {
+                int pg = ent[j];
+                if (pg < 0 || pg >= p.num_pages) {
+                    raise_status(p, kErrBounds);
+                    pg = -1;
+                }
+                pages[i] = pg;
+            }
+        }
+    }
+};
+
+template <int D, bool kBF16, int MT, int NT, int NBUF, int NW = kNW>
+__global__ void __launch_bounds__(NW * 32)
 decode_mma_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p) {
-    using S = MmaShape<D, MT, NT, NBUF>;
+    using S = MmaShape<D, MT, NT, NBUF, NW>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::OFF_BARS);
     int* pages = reinterpret_cast<int*>(smem + S::OFF_PAGES);
     uint8_t* qs = smem + S::OFF_Q;
     float* wm = reinterpret_cast<float*>(smem + S::OFF_ML);
-    float* wl = wm + kNW * S::MROWS;
+    float* wl = wm + NW * S::MROWS;
     int* flag = reinterpret_cast<int*>(smem + S::OFF_FLAG);
 
+    SpecPages<NW * 32> spec;
+    spec.load(p);
     CtaWork w;
     if (!cta_setup<D>(p, w)) return;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
         prefetch_tmap(&tmap);
-        for (int i = 0; i < kNW * NBUF; ++i) mbar_init(smem_u32(bars + i), 1);
+        for (int i = 0; i < NW * NBUF; ++i) mbar_init(smem_u32(bars + i), 1);
         fence_barrier_init();
     }
-    load_cta_pages(p, w, pages);
+    if (spec.on)
+        spec.store(p, w, pages);
+    else
+        load_cta_pages(p, w, pages);
 
     // stage the M query rows (zero padding rows) for ldmatrix
     {
@@ -81,16 +126,14 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p
     __syncthreads();
 
     const int nst = (w.t1 - w.t0 + kStageTok - 1) / kStageTok;
-    const int my_n = nst > warp ? (nst - warp + kNW - 1) / kNW : 0;
+    const int my_n = nst > warp ? (nst - warp + NW - 1) / NW : 0;
     uint8_t* ring_gen = smem + warp * NBUF * S::STAGE;
     const uint32_t ring = smem_u32(ring_gen);
     const uint32_t bar0 = smem_u32(bars + warp * NBUF);
     const uint64_t pol = policy_evict_first();
-    if (kPrefetch > 0 && lane == 0)
-        for (int k = NBUF; k < NBUF + kPrefetch; ++k) prefetch_stage(&tmap, p, w, pages, warp + k * kNW);
     if (lane == 0)
         for (int k = 0; k < NBUF && k < my_n; ++k)
-            issue_stage<D, 2>(&tmap, p, w, pages, warp + k * kNW, ring + k * S::STAGE, bar0 + 8 * k, pol);
+            issue_stage<D, 2>(&tmap, p, w, pages, warp + k * NW, ring + k * S::STAGE, bar0 + 8 * k, pol);
 
     MmaWarp<D, kBF16, MT, NT> wp;
     wp.load_q(smem_u32(qs), S::QSTRIDE, lane);
@@ -105,7 +148,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p
             break;
         }
         consumed = k + 1;
-        const int stage = warp + k * kNW;
+        const int stage = warp + k * NW;
         const int tok0 = w.t0 + stage * kStageTok;
         int nvalid = min(kStageTok, w.t1 - tok0);
         if (page_of(p, w, pages, tok0) < 0) nvalid = 0;
@@ -115,9 +158,8 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p
                    [&](int row, int kt) { return row_sees(p, L, row, tok0 + kt); }, lane);
         __syncwarp();
         if (lane == 0 && k + NBUF < my_n) {
-            if (kPrefetch > 0) prefetch_stage(&tmap, p, w, pages, warp + (k + NBUF + kPrefetch) * kNW);
             fence_proxy_async();
-            issue_stage<D, 2>(&tmap, p, w, pages, warp + (k + NBUF) * kNW, st, bar0 + 8 * buf, pol);
+            issue_stage<D, 2>(&tmap, p, w, pages, warp + (k + NBUF) * NW, st, bar0 + 8 * buf, pol);
         }
     }
     if (timed_out) {
@@ -133,7 +175,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p
     float* O = reinterpret_cast<float*>(smem);
     wp.store(O + warp * S::MROWS * S::OSTRIDE, wm + warp * S::MROWS, wl + warp * S::MROWS, S::OSTRIDE, lane);
     __syncthreads();
-    cta_finish<D, S::OSTRIDE>(p, w, O, wm, wl, S::MROWS, flag);
+    cta_finish<D, S::OSTRIDE, NW>(p, w, O, wm, wl, S::MROWS, flag);
 }
 
 // Query blocks of 17..32 rows (M = sq * Hq/Hkv).  One warp holding both
