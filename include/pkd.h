@@ -46,8 +46,8 @@ typedef enum {
 /* Flags for pkd_paged_decode. */
 #define PKD_FLAG_CAUSAL 1u      /* causal mask inside the query block, exact per-token window */
 #define PKD_FLAG_MMA_SMALL_M 2u /* tensor cores for sq*Hq/Hkv < 16 (the default for 16-bit caches) */
-#define PKD_FLAG_FMA 4u         /* CUDA cores instead (only when sq*Hq/Hkv <= 8; always for fp8) */
-#define PKD_FLAG_GRID 8u        /* one CTA per Split-KV chunk instead of the persistent flat partition */
+#define PKD_FLAG_FMA 4u         /* CUDA cores instead (only when sq*Hq/Hkv <= 8) */
+#define PKD_FLAG_GRID 8u        /* the chunked grid: one CTA per Split-KV chunk */
 #define PKD_FLAG_FLAT 16u       /* the persistent flat partition whatever the shapes (batch <= 1024) */
 #define PKD_FLAG_BALANCED 32u   /* the persistent per-CTA partition (16-bit caches, tensor cores) */
 
@@ -131,13 +131,18 @@ pkd_status pkd_workspace_check(void* workspace, size_t workspace_bytes, void* st
  *
  * Split-KV [FA num_splits]: the keys of a (request, kv head) may be shared
  * between several workers whose partial results are merged by LSE inside
- * the same launch.  For batch <= 1024 a persistent grid gives every warp an
- * equal slice of all requests' keys laid end to end; otherwise (or with
- * PKD_FLAG_GRID) one CTA takes each chunk of chunk_tokens keys.
+ * the same launch.  16-bit caches with M = sq * num_heads / num_kv_heads
+ * <= 16 run on a chunked grid, one CTA per chunk of chunk_tokens keys
+ * (0: chosen by the library).  fp8 caches and M > 16 run, for batch <= 1024,
+ * on a persistent grid that gives every warp an equal slice of all requests'
+ * keys laid end to end.  PKD_FLAG_GRID, PKD_FLAG_FLAT and PKD_FLAG_BALANCED
+ * (a persistent grid with an equal slice per CTA) force a kernel;
+ * pkd_paged_decode_kernel_name says which one a call launches.
  *
  * Limits: head_dim 64 or 128; page_size a multiple of 16; num_heads a
- * multiple of num_kv_heads; sq * num_heads / num_kv_heads <= 32 (<= 8 for fp8);
- * fp8 caches need head_dim 128.  Anything else: PKD_EUNSUPPORTED.  After a
+ * multiple of num_kv_heads; M <= 32 on tensor cores, <= 8 on CUDA cores
+ * (PKD_FLAG_FMA); fp8 caches need head_dim 128, and M > 16 with fp8 needs the
+ * per-warp persistent grid.  Anything else: PKD_EUNSUPPORTED.  After a
  * PKD_ETIMEOUT, zero the workspace again before reusing it.
  */
 pkd_status pkd_paged_decode(const void* q, pkd_dtype q_dtype,

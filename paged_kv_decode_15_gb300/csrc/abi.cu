@@ -74,12 +74,13 @@ pkd_status make_plan(int B, int sq, int Hq, int Hkv, int D, int P, int max_kv_le
     pl.G = Hq / Hkv;
     pl.M = sq * pl.G;
     const int M = pl.M;
-    // The persistent flat partition balances few or long units best and is the
-    // only home of the fp8 tensor-core warp and of the split row tiles (M > 16);
-    // with many short units of a 16-bit cache and M <= 16 the chunked grid is
-    // faster (gqa_decode_b64: 108.6 vs 126.9 us).  PKD_FLAG_GRID forces the grid.
-    const bool many_units = (long long)B * Hkv >= 256;
-    const bool flat_only = kv == PKD_FP8_E4M3 || (long long)sq * (Hq / Hkv) > 16;
+    // Kernel choice (measured): 16-bit caches with M <= 16 run on the chunked
+    // grid, whose hardware CTA scheduling keeps every SM busy to the end
+    // (gqa_decode_b64: 100.6 us against 126 us per-warp and 116 us per-CTA
+    // partitions; tiny problems: 8.5 against 36.5 us).  fp8 caches and M > 16
+    // default to the persistent per-warp partition.  PKD_FLAG_GRID,
+    // PKD_FLAG_FLAT and PKD_FLAG_BALANCED force a kernel.
+    const bool flat_default = kv == PKD_FP8_E4M3 || (long long)sq * (Hq / Hkv) > 16;
     if (((flags & PKD_FLAG_GRID) != 0) + ((flags & PKD_FLAG_FLAT) != 0) + ((flags & PKD_FLAG_BALANCED) != 0) > 1)
         return fail(PKD_EINVAL, "PKD_FLAG_GRID, PKD_FLAG_FLAT and PKD_FLAG_BALANCED exclude each other");
     pl.bal = false;
@@ -89,11 +90,14 @@ pkd_status make_plan(int B, int sq, int Hq, int Hkv, int D, int P, int max_kv_le
         pl.bal = true;
     }
     pl.flat = !pl.bal && B <= pkd::kFlatMaxBatch && !(flags & PKD_FLAG_GRID) &&
-              ((flags & PKD_FLAG_FLAT) || flat_only || !many_units);
-    if (kv == PKD_FP8_E4M3 && (!pl.flat || (flags & PKD_FLAG_FMA))) {
-        // the chunked grid reads fp8 on CUDA cores only
+              ((flags & PKD_FLAG_FLAT) || flat_default);
+    if (kv == PKD_FP8_E4M3 && (flags & PKD_FLAG_FMA)) {
         if (M > 8) return fail(PKD_EUNSUPPORTED, "fp8 on CUDA cores supports sq*num_heads/num_kv_heads <= 8 (got %d)", M);
         pl.mma = false;
+    } else if (kv == PKD_FP8_E4M3 && !pl.flat && M > 16) {
+        return fail(PKD_EUNSUPPORTED,
+                    "fp8 caches with more than 16 query rows per kv head (got %d) run on the flat partition only "
+                    "(batch <= %d, no PKD_FLAG_GRID)", M, pkd::kFlatMaxBatch);
     } else if (flags & PKD_FLAG_FMA) {
         if (M > 8) return fail(PKD_EUNSUPPORTED, "the CUDA-core kernel supports sq*num_heads/num_kv_heads <= 8 (got %d)", M);
         pl.mma = false;
@@ -410,6 +414,8 @@ pkd_status pkd_paged_decode(const void* q, pkd_dtype q_dtype, const void* kv_cac
         e = kv_dtype == PKD_BF16   ? pkd::launch_flat_fma_bf16(head_dim, pl.lpt, pl.mr, tmap, p, max_ctas, s)
             : kv_dtype == PKD_FP16 ? pkd::launch_flat_fma_fp16(head_dim, pl.lpt, pl.mr, tmap, p, max_ctas, s)
                                    : pkd::launch_flat_fma_fp8(head_dim, pl.lpt, pl.mr, tmap, p, max_ctas, s);
+    else if (pl.mma && kv_dtype == PKD_FP8_E4M3)
+        e = pkd::launch_decode_mma_fp8(head_dim, pl.mt, pl.nt, tmap, p, dim3(pl.max_splits, num_kv_heads, batch), s);
     else if (pl.mma)
         e = pkd::launch_decode_mma(head_dim, kv_dtype == PKD_BF16, pl.mt, pl.nt, tmap, p,
                                    dim3(pl.max_splits, num_kv_heads, batch), s);

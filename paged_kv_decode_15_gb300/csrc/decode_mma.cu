@@ -7,11 +7,12 @@ namespace pkd {
 constexpr int kMmaNbuf = 2;
 constexpr int kGridWarps = 4;  // warps per CTA of the one-tile kernel
 constexpr int kPairNbuf = 4;  // per warp pair: the same 64 KiB of ring per CTA as four rings of two
+constexpr int kFp8Nbuf = 3;   // 4 KiB e4m3 stages: three per warp, beside 4 KiB of widening scratch
 
-template <int D, bool kBF16, int MT, int NT>
+template <class W, int D, int ELT, int NBUF>
 static cudaError_t launch_one(const CUtensorMap& tmap, const DecodeParams& p, dim3 grid, cudaStream_t stream) {
-    using S = MmaShape<D, MT, NT, kMmaNbuf, kGridWarps>;
-    auto kern = decode_mma_kernel<D, kBF16, MT, NT, kMmaNbuf, kGridWarps>;
+    using S = MmaShape<W, D, ELT, NBUF, kGridWarps>;
+    auto kern = decode_mma_kernel<W, D, ELT, NBUF, kGridWarps>;
     static bool configured = false;  // benign race: the attribute call is idempotent
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
@@ -36,21 +37,20 @@ static cudaError_t launch_pair(const CUtensorMap& tmap, const DecodeParams& p, d
     return cudaGetLastError();
 }
 
-int decode_mma_smem(int D, int MT, int NT) {
-#define PKD_MMA_SMEM(d, mt, nt) \
-    if (D == d && MT == mt && NT == nt) return MmaShape<d, mt, nt, kMmaNbuf>::SMEM;
-    PKD_MMA_SMEM(128, 1, 1) PKD_MMA_SMEM(128, 1, 2) PKD_MMA_SMEM(64, 1, 1) PKD_MMA_SMEM(64, 1, 2)
-    if (MT == 2) return D == 128 ? PairShape<128, kPairNbuf>::SMEM : D == 64 ? PairShape<64, kPairNbuf>::SMEM : -1;
-#undef PKD_MMA_SMEM
-    return -1;
+
+cudaError_t launch_decode_mma_fp8(int D, int MT, int NT, const CUtensorMap& tmap, const DecodeParams& p, dim3 grid,
+                                  cudaStream_t stream) {
+    if (D == 128 && MT == 1 && NT == 1) return launch_one<Fp8MmaWarp<1, 1>, 128, 1, kFp8Nbuf>(tmap, p, grid, stream);
+    if (D == 128 && MT == 1 && NT == 2) return launch_one<Fp8MmaWarp<1, 2>, 128, 1, kFp8Nbuf>(tmap, p, grid, stream);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_decode_mma(int D, bool bf16, int MT, int NT, const CUtensorMap& tmap,
                               const DecodeParams& p, dim3 grid, cudaStream_t stream) {
-#define PKD_MMA_CASE(d, mt, nt)                                                              \
-    if (D == d && MT == mt && NT == nt)                                                      \
-        return bf16 ? launch_one<d, true, mt, nt>(tmap, p, grid, stream)                     \
-                    : launch_one<d, false, mt, nt>(tmap, p, grid, stream);
+#define PKD_MMA_CASE(d, mt, nt)                                                                          \
+    if (D == d && MT == mt && NT == nt)                                                                  \
+        return bf16 ? launch_one<MmaWarp<d, true, mt, nt>, d, 2, kMmaNbuf>(tmap, p, grid, stream)         \
+                    : launch_one<MmaWarp<d, false, mt, nt>, d, 2, kMmaNbuf>(tmap, p, grid, stream);
     PKD_MMA_CASE(128, 1, 1) PKD_MMA_CASE(128, 1, 2) PKD_MMA_CASE(64, 1, 1) PKD_MMA_CASE(64, 1, 2)
     // 17..32 rows: warp pairs sharing one ring, 16 rows per warp
     if (MT == 2 && D == 128) return bf16 ? launch_pair<128, true>(tmap, p, grid, stream)

@@ -14,27 +14,30 @@
 // from the cache's own [pages, Hkv, P, 2*D] layout without any repacking.
 #pragma once
 
+#include "fp8_warp.cuh"
 #include "mma_warp.cuh"
 
 namespace pkd {
 
-template <int D, int MT, int NT, int NBUF, int NW = kNW>
+// Shared memory of a grid CTA: NW rings of NBUF stages (reused for the warps'
+// O at the end), barriers, the page list, the q rows staged for the warps
+// (W::kCtaQ), per-warp row statistics and per-warp scratch (W::kScratchBytes).
+template <class W, int D, int ELT, int NBUF, int NW = kNW>
 struct MmaShape {
-    static constexpr int ELT = 2;
-    static constexpr int ROWB = D * ELT;
-    static constexpr int KBOX = ROWB / 128;
+    static constexpr int KBOX = D * ELT / 128;
     static constexpr int HALF = KBOX * 2048;
     static constexpr int STAGE = 2 * HALF;
-    static constexpr int MROWS = MT * 16;
+    static constexpr int MROWS = W::MROWS;
     static constexpr int QSTRIDE = D * 2 + 16;           // bytes per staged q row
     static constexpr int OSTRIDE = D + 4;                // floats per merge row
     static constexpr int RING = NW * NBUF * STAGE;
     static constexpr int MERGE = NW * MROWS * OSTRIDE * 4;
     static constexpr int BIG = RING > MERGE ? RING : MERGE;
-    static constexpr int OFF_BARS = BIG;
+    static constexpr int OFF_SCR = BIG;                  // per-warp scratch, 1 KiB granules
+    static constexpr int OFF_BARS = OFF_SCR + NW * W::kScratchBytes;
     static constexpr int OFF_PAGES = OFF_BARS + NW * NBUF * 8;
     static constexpr int OFF_Q = OFF_PAGES + kMaxCtaPages * 4;
-    static constexpr int OFF_ML = OFF_Q + MROWS * QSTRIDE;
+    static constexpr int OFF_ML = OFF_Q + (W::kCtaQ ? MROWS * QSTRIDE : 0);
     static constexpr int OFF_FLAG = OFF_ML + 2 * NW * MROWS * 4;
     static constexpr int SMEM = OFF_FLAG + 16 + 1024;    // + slack to align the base to 1 KiB
 };
@@ -79,10 +82,13 @@ struct SpecPages {
     }
 };
 
-template <int D, bool kBF16, int MT, int NT, int NBUF, int NW = kNW>
+// W: MmaWarp (16-bit caches; q rows staged once for the CTA's warps) or
+// Fp8MmaWarp (e4m3 caches; q fragments loaded by each warp, V widened in the
+// warp's scratch).
+template <class W, int D, int ELT, int NBUF, int NW = kNW>
 __global__ void __launch_bounds__(NW * 32)
 decode_mma_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p) {
-    using S = MmaShape<D, MT, NT, NBUF, NW>;
+    using S = MmaShape<W, D, ELT, NBUF, NW>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::OFF_BARS);
@@ -109,7 +115,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p
         load_cta_pages(p, w, pages);
 
     // stage the M query rows (zero padding rows) for ldmatrix
-    {
+    if constexpr (W::kCtaQ) {
         constexpr int VPR = D * 2 / 16;  // 16-byte vectors per row
         const uint4* qg = reinterpret_cast<const uint4*>(p.q);
         for (int e = tid; e < S::MROWS * VPR; e += blockDim.x) {
@@ -133,10 +139,14 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p
     const uint64_t pol = policy_evict_first();
     if (lane == 0)
         for (int k = 0; k < NBUF && k < my_n; ++k)
-            issue_stage<D, 2>(&tmap, p, w, pages, warp + k * NW, ring + k * S::STAGE, bar0 + 8 * k, pol);
+            issue_stage<D, ELT>(&tmap, p, w, pages, warp + k * NW, ring + k * S::STAGE, bar0 + 8 * k, pol);
 
-    MmaWarp<D, kBF16, MT, NT> wp;
-    wp.load_q(smem_u32(qs), S::QSTRIDE, lane);
+    W wp;
+    wp.setup(smem + S::OFF_SCR + warp * W::kScratchBytes);
+    if constexpr (W::kCtaQ)
+        wp.load_q(smem_u32(qs), S::QSTRIDE, lane);
+    else
+        wp.load_q(p, w.b, w.hk, lane);
     wp.reset();
     const int L = w.L;
 
@@ -153,13 +163,13 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p
         int nvalid = min(kStageTok, w.t1 - tok0);
         if (page_of(p, w, pages, tok0) < 0) nvalid = 0;
         const uint32_t st = ring + buf * S::STAGE;
-        if (nvalid < kStageTok) zero_tail_v<D, 2>(ring_gen + buf * S::STAGE, nvalid, lane);
+        if (nvalid < kStageTok) zero_tail_v<D, ELT>(ring_gen + buf * S::STAGE, nvalid, lane);
         wp.consume(st, S::HALF, nvalid, nvalid < kStageTok || p.causal, p.scale_log2, 0.f,
                    [&](int row, int kt) { return row_sees(p, L, row, tok0 + kt); }, lane);
         __syncwarp();
         if (lane == 0 && k + NBUF < my_n) {
             fence_proxy_async();
-            issue_stage<D, 2>(&tmap, p, w, pages, warp + (k + NBUF) * NW, st, bar0 + 8 * buf, pol);
+            issue_stage<D, ELT>(&tmap, p, w, pages, warp + (k + NBUF) * NW, st, bar0 + 8 * buf, pol);
         }
     }
     if (timed_out) {

@@ -17,6 +17,7 @@ struct Fp8MmaWarp : MmaWarp<128, false, MT, NT> {
     using Base = MmaWarp<128, false, MT, NT>;
     static constexpr int kWide = 2 * 2048;  // one fp16 V tile: two 128-byte boxes of 16 rows
     static constexpr int kScratchBytes = kWide;
+    static constexpr bool kCtaQ = false;  // e4m3 q fragments come straight from global memory
     uint32_t q8[MT][4][4];                  // e4m3 A fragments, 4 k-steps of 32
     uint32_t wide = 0;
     uint8_t* wide_gen = nullptr;

@@ -12,12 +12,14 @@ struct DecodeParams;
 
 // Dynamic shared memory of a decode kernel variant (bytes), or -1 if the
 // variant is not built.
-int decode_mma_smem(int D, int MT, int NT);
 int decode_fma_smem(int D, int kvt, int LPT, int MR);
 
 // Launch one decode kernel variant on `stream`; grid = (max_splits, Hkv, B).
 cudaError_t launch_decode_mma(int D, bool bf16, int MT, int NT, const CUtensorMap& tmap,
                               const DecodeParams& p, dim3 grid, cudaStream_t stream);
+// e4m3 caches on tensor cores in the chunked grid (M <= 16)
+cudaError_t launch_decode_mma_fp8(int D, int MT, int NT, const CUtensorMap& tmap, const DecodeParams& p, dim3 grid,
+                                  cudaStream_t stream);
 cudaError_t launch_decode_fma(int D, int kvt, int LPT, int MR, const CUtensorMap& tmap,
                               const DecodeParams& p, dim3 grid, cudaStream_t stream);
 

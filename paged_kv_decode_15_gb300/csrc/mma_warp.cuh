@@ -63,6 +63,7 @@ struct MmaWarp {
     // per-warp shared memory beyond the ring: the staged q rows (1 KiB granules)
     static constexpr int kScratchBytes = kQSmem ? (MROWS * QSTRIDE + 1023) / 1024 * 1024 : 0;
     static constexpr int kNbuf = 2;  // ring depth per warp (three CTAs of four warps fit an SM)
+    static constexpr bool kCtaQ = true;  // grid kernels stage q once for the CTA's warps
 
     __device__ __forceinline__ void setup(uint8_t* scratch) {
         qs_gen = scratch;

@@ -48,11 +48,11 @@ def test_workspace_plan_is_a_host_function(lib):
     # chunked grid, explicit chunk: 4096 / 256 = 16 splits -> partials [512 units, 16, 4 rows, 128] fp32
     m = pkd.workspace_size(64, 1, 32, 8, 128, 16, 4096, pkd.BF16, chunk_tokens=256, flags=pkd.FLAG_GRID)
     assert m >= 512 * 16 * 4 * 128 * 4
-    # flat partition (few units: 8 x 8 < 256): two partial slots per worker warp, independent of the lengths
-    f1 = pkd.workspace_size(8, 1, 32, 8, 128, 16, 4096, pkd.BF16)
-    f2 = pkd.workspace_size(8, 1, 32, 8, 128, 16, 131072, pkd.BF16)
+    # flat partition: two partial slots per worker warp, independent of the lengths
+    f1 = pkd.workspace_size(8, 1, 32, 8, 128, 16, 4096, pkd.BF16, flags=pkd.FLAG_FLAT)
+    f2 = pkd.workspace_size(8, 1, 32, 8, 128, 16, 131072, pkd.BF16, flags=pkd.FLAG_FLAT)
     assert f1 == f2 and f1 >= 2048 * 2 * 4 * 128 * 4
-    # many short units of a 16-bit cache with M <= 16 take the chunked grid by default ...
+    # 16-bit caches with M <= 16 take the chunked grid by default ...
     assert n == pkd.workspace_size(64, 1, 32, 8, 128, 16, 4096, pkd.BF16, flags=pkd.FLAG_GRID)
     # ... and fp8 or M > 16 stay on the flat partition whatever the batch
     assert pkd.workspace_size(64, 1, 32, 8, 128, 16, 4096, pkd.FP8_E4M3) == \
@@ -69,7 +69,7 @@ def test_workspace_plan_is_a_host_function(lib):
     ((2, 1, 8, 2, 96, 16, 100, pkd.BF16), "head_dim"),
     ((2, 1, 8, 2, 128, 8, 100, pkd.BF16), "page_size"),
     ((2, 4, 32, 8, 128, 16, 100, pkd.FP8_E4M3, 0, 0, pkd.FLAG_FMA), "fp8"),
-    ((2, 4, 32, 8, 128, 16, 100, pkd.FP8_E4M3, 0, 0, pkd.FLAG_GRID), "fp8"),
+    ((2, 8, 32, 8, 128, 16, 100, pkd.FP8_E4M3, 0, 0, pkd.FLAG_GRID), "fp8"),
     ((2, 16, 32, 8, 128, 16, 100, pkd.BF16), "> 32"),
     ((2, 1, 8, 2, 64, 16, 100, pkd.FP8_E4M3), "head_dim 128"),
 ])
@@ -144,11 +144,13 @@ def test_kernel_name_follows_the_plan(lib):
     args = (64, 1, 32, 8, 128, 16, 4096)
     assert pkd.kernel_name(*args, pkd.BF16) == "chunked grid, tensor cores"
     assert pkd.kernel_name(*args, pkd.BF16, flags=pkd.FLAG_FLAT) == "persistent flat partition, tensor cores"
-    assert pkd.kernel_name(8, 1, 32, 8, 128, 16, 4096, pkd.BF16) == "persistent flat partition, tensor cores"
+    assert pkd.kernel_name(8, 1, 32, 8, 128, 16, 4096, pkd.BF16) == "chunked grid, tensor cores"
+    assert pkd.kernel_name(8, 8, 32, 8, 128, 16, 4096, pkd.BF16) == "persistent flat partition, tensor cores"
     assert pkd.kernel_name(*args, pkd.BF16, flags=pkd.FLAG_FMA | pkd.FLAG_GRID) == "chunked grid, CUDA cores"
     assert pkd.kernel_name(*args, pkd.FP8_E4M3) == "persistent flat partition, tensor cores"
-    assert pkd.kernel_name(*args, pkd.FP8_E4M3, flags=pkd.FLAG_GRID) == "chunked grid, CUDA cores"
-    assert pkd.kernel_name(2048, 1, 32, 8, 128, 16, 4096, pkd.FP8_E4M3) == "chunked grid, CUDA cores"
+    assert pkd.kernel_name(*args, pkd.FP8_E4M3, flags=pkd.FLAG_GRID) == "chunked grid, tensor cores"
+    assert pkd.kernel_name(*args, pkd.FP8_E4M3, flags=pkd.FLAG_GRID | pkd.FLAG_FMA) == "chunked grid, CUDA cores"
+    assert pkd.kernel_name(2048, 1, 32, 8, 128, 16, 4096, pkd.FP8_E4M3) == "chunked grid, tensor cores"
     with pytest.raises(pkd.PkdError, match="head_dim"):
         pkd.kernel_name(2, 1, 8, 2, 96, 16, 100, pkd.BF16)
     with pytest.raises(pkd.PkdError, match="exclude"):
