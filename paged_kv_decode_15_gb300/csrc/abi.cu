@@ -74,13 +74,13 @@ pkd_status make_plan(int B, int sq, int Hq, int Hkv, int D, int P, int max_kv_le
     pl.G = Hq / Hkv;
     pl.M = sq * pl.G;
     const int M = pl.M;
-    // Kernel choice (measured): 16-bit caches with M <= 16 run on the chunked
-    // grid, whose hardware CTA scheduling keeps every SM busy to the end
-    // (gqa_decode_b64: 100.6 us against 126 us per-warp and 116 us per-CTA
-    // partitions; tiny problems: 8.5 against 36.5 us).  fp8 caches and M > 16
-    // default to the persistent per-warp partition.  PKD_FLAG_GRID,
-    // PKD_FLAG_FLAT and PKD_FLAG_BALANCED force a kernel.
-    const bool flat_default = kv == PKD_FP8_E4M3 || (long long)sq * (Hq / Hkv) > 16;
+    // Kernel choice (measured): M <= 16 runs on the chunked grid, whose
+    // hardware CTA scheduling keeps every SM busy to the end (gqa_decode_b64:
+    // 100.6 us against 126 us per-warp and 116 us per-CTA partitions;
+    // fp8_long_b8: 481.5 against 491.3 us per-warp; tiny problems: 8.5 against
+    // 36.5 us).  M > 16 defaults to the persistent per-warp partition.
+    // PKD_FLAG_GRID, PKD_FLAG_FLAT and PKD_FLAG_BALANCED force a kernel.
+    const bool flat_default = (long long)sq * (Hq / Hkv) > 16;
     if (((flags & PKD_FLAG_GRID) != 0) + ((flags & PKD_FLAG_FLAT) != 0) + ((flags & PKD_FLAG_BALANCED) != 0) > 1)
         return fail(PKD_EINVAL, "PKD_FLAG_GRID, PKD_FLAG_FLAT and PKD_FLAG_BALANCED exclude each other");
     pl.bal = false;

@@ -54,9 +54,10 @@ def test_workspace_plan_is_a_host_function(lib):
     assert f1 == f2 and f1 >= 2048 * 2 * 4 * 128 * 4
     # 16-bit caches with M <= 16 take the chunked grid by default ...
     assert n == pkd.workspace_size(64, 1, 32, 8, 128, 16, 4096, pkd.BF16, flags=pkd.FLAG_GRID)
-    # ... and fp8 or M > 16 stay on the flat partition whatever the batch
+    # ... fp8 caches too ...
     assert pkd.workspace_size(64, 1, 32, 8, 128, 16, 4096, pkd.FP8_E4M3) == \
-        pkd.workspace_size(64, 1, 32, 8, 128, 16, 131072, pkd.FP8_E4M3)
+        pkd.workspace_size(64, 1, 32, 8, 128, 16, 4096, pkd.FP8_E4M3, flags=pkd.FLAG_GRID)
+    # ... and M > 16 stays on the flat partition whatever the lengths
     assert pkd.workspace_size(64, 8, 32, 8, 128, 16, 4096, pkd.BF16) == \
         pkd.workspace_size(64, 8, 32, 8, 128, 16, 131072, pkd.BF16)
     # batches above the flat kernel's table size use the chunked grid
@@ -147,7 +148,8 @@ def test_kernel_name_follows_the_plan(lib):
     assert pkd.kernel_name(8, 1, 32, 8, 128, 16, 4096, pkd.BF16) == "chunked grid, tensor cores"
     assert pkd.kernel_name(8, 8, 32, 8, 128, 16, 4096, pkd.BF16) == "persistent flat partition, tensor cores"
     assert pkd.kernel_name(*args, pkd.BF16, flags=pkd.FLAG_FMA | pkd.FLAG_GRID) == "chunked grid, CUDA cores"
-    assert pkd.kernel_name(*args, pkd.FP8_E4M3) == "persistent flat partition, tensor cores"
+    assert pkd.kernel_name(*args, pkd.FP8_E4M3) == "chunked grid, tensor cores"
+    assert pkd.kernel_name(64, 8, 32, 8, 128, 16, 4096, pkd.FP8_E4M3) == "persistent flat partition, tensor cores"
     assert pkd.kernel_name(*args, pkd.FP8_E4M3, flags=pkd.FLAG_GRID) == "chunked grid, tensor cores"
     assert pkd.kernel_name(*args, pkd.FP8_E4M3, flags=pkd.FLAG_GRID | pkd.FLAG_FMA) == "chunked grid, CUDA cores"
     assert pkd.kernel_name(2048, 1, 32, 8, 128, 16, 4096, pkd.FP8_E4M3) == "chunked grid, tensor cores"
