@@ -131,9 +131,10 @@ pkd_status pkd_workspace_check(void* workspace, size_t workspace_bytes, void* st
  *
  * Split-KV [FA num_splits]: the keys of a (request, kv head) may be shared
  * between several workers whose partial results are merged by LSE inside
- * the same launch.  M = sq * num_heads / num_kv_heads <= 16 runs on a
- * chunked grid, one CTA per chunk of chunk_tokens keys (0: chosen by the
- * library).  M > 16 runs, for batch <= 1024, on a persistent grid that gives
+ * the same launch.  By default a chunked grid runs one CTA per chunk of
+ * chunk_tokens keys (0: chosen by the library); for M = sq * num_heads /
+ * num_kv_heads > 16 two warps share each chunk's stages, 16 rows each.  fp8
+ * caches with M > 16 run, for batch <= 1024, on a persistent grid that gives
  * every warp an equal slice of all requests' keys laid end to end.  PKD_FLAG_GRID, PKD_FLAG_FLAT and PKD_FLAG_BALANCED
  * (a persistent grid with an equal slice per CTA) force a kernel;
  * pkd_paged_decode_kernel_name says which one a call launches.

@@ -40,11 +40,9 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 int elt_bytes(pkd_dtype dt) { return dt == PKD_FP8_E4M3 ? 1 : dt == PKD_FP32 ? 4 : 2; }
 
 // ---------------------------------------------------------------- plan
-// Split-KV aims for about this many CTAs: measured on gqa_decode_b64 (M = 4)
-// 2048 (1024-key chunks) beats 1024, 1536 or 3072; the warp-pair kernel
-// (M > 16) does better with half as many, longer chunks.
+// Split-KV aims for about this many CTAs with one-tile kernels: measured on
+// gqa_decode_b64 (M = 4) 2048 (1024-key chunks) beats 512- to 2048-key chunks.
 constexpr int kTargetCtas = 2048;
-constexpr int kTargetCtasPair = 1024;
 constexpr int kMaxChunk = 4096;    // and never puts more keys than this in one chunk
 constexpr size_t kHeader = 256;    // workspace status word lives in the first bytes
 
@@ -74,13 +72,14 @@ pkd_status make_plan(int B, int sq, int Hq, int Hkv, int D, int P, int max_kv_le
     pl.G = Hq / Hkv;
     pl.M = sq * pl.G;
     const int M = pl.M;
-    // Kernel choice (measured): M <= 16 runs on the chunked grid, whose
-    // hardware CTA scheduling keeps every SM busy to the end (gqa_decode_b64:
-    // 100.6 us against 126 us per-warp and 116 us per-CTA partitions;
-    // fp8_long_b8: 481.5 against 491.3 us per-warp; tiny problems: 8.5 against
-    // 36.5 us).  M > 16 defaults to the persistent per-warp partition.
+    // Kernel choice (measured): the chunked grid, whose hardware CTA
+    // scheduling keeps every SM busy to the end (gqa_decode_b64: 101 us
+    // against 124 us per-warp and 115 us per-CTA partitions; fp8_long_b8: 482
+    // against 489 us; query_block_sq8 with warp pairs: 193 against 214 us;
+    // tiny problems: 8.5 against 36.5 us).  fp8 caches with M > 16 have no
+    // warp-pair kernel and take the persistent per-warp partition.
     // PKD_FLAG_GRID, PKD_FLAG_FLAT and PKD_FLAG_BALANCED force a kernel.
-    const bool flat_default = (long long)sq * (Hq / Hkv) > 16;
+    const bool flat_default = kv == PKD_FP8_E4M3 && (long long)sq * (Hq / Hkv) > 16;
     if (((flags & PKD_FLAG_GRID) != 0) + ((flags & PKD_FLAG_FLAT) != 0) + ((flags & PKD_FLAG_BALANCED) != 0) > 1)
         return fail(PKD_EINVAL, "PKD_FLAG_GRID, PKD_FLAG_FLAT and PKD_FLAG_BALANCED exclude each other");
     pl.bal = false;
@@ -125,8 +124,11 @@ pkd_status make_plan(int B, int sq, int Hq, int Hkv, int D, int P, int max_kv_le
             return fail(PKD_EINVAL, "chunk_tokens %d spans more than %d pages", chunk_tokens, pkd::kMaxCtaPages);
         pl.chunk = chunk_tokens;
     } else {
-        const int target = pl.mma && pl.mt == 2 ? kTargetCtasPair : kTargetCtas;
-        int splits = (target + units - 1) / units;
+        // one-tile kernels: about kTargetCtas CTAs; warp pairs (M > 16): as few
+        // chunks as the chunk limit allows, since each partial is M x D floats
+        // (query_block_sq8: 4096-key chunks 193 us, 2048 216 us, 1024 246 us)
+        const bool pair = pl.mma && pl.mt == 2 && !pl.flat && !pl.bal;
+        int splits = pair ? 1 : (kTargetCtas + units - 1) / units;
         const int by_len = (pl.max_vis + kMaxChunk - 1) / kMaxChunk;
         if (by_len > splits) splits = by_len;
         if (splits < 1) splits = 1;

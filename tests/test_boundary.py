@@ -57,9 +57,14 @@ def test_workspace_plan_is_a_host_function(lib):
     # ... fp8 caches too ...
     assert pkd.workspace_size(64, 1, 32, 8, 128, 16, 4096, pkd.FP8_E4M3) == \
         pkd.workspace_size(64, 1, 32, 8, 128, 16, 4096, pkd.FP8_E4M3, flags=pkd.FLAG_GRID)
-    # ... and M > 16 stays on the flat partition whatever the lengths
-    assert pkd.workspace_size(64, 8, 32, 8, 128, 16, 4096, pkd.BF16) == \
-        pkd.workspace_size(64, 8, 32, 8, 128, 16, 131072, pkd.BF16)
+    # ... 16-bit M > 16 too (warp pairs, as few chunks as the 4096-key limit allows:
+    # 8192 keys -> 2 chunks -> partials [512 units, 2, 32 rows, 128] fp32) ...
+    w = pkd.workspace_size(64, 8, 32, 8, 128, 16, 8192, pkd.BF16)
+    assert w == pkd.workspace_size(64, 8, 32, 8, 128, 16, 8192, pkd.BF16, chunk_tokens=4096, flags=pkd.FLAG_GRID)
+    assert 512 * 2 * 32 * 128 * 4 <= w < 512 * 3 * 32 * 128 * 4
+    # ... while fp8 with M > 16 stays on the flat partition whatever the lengths
+    assert pkd.workspace_size(64, 8, 32, 8, 128, 16, 4096, pkd.FP8_E4M3) == \
+        pkd.workspace_size(64, 8, 32, 8, 128, 16, 131072, pkd.FP8_E4M3)
     # batches above the flat kernel's table size use the chunked grid
     assert pkd.workspace_size(2048, 1, 32, 8, 128, 16, 4096, pkd.BF16) == \
         pkd.workspace_size(2048, 1, 32, 8, 128, 16, 4096, pkd.BF16, flags=pkd.FLAG_GRID)
@@ -146,7 +151,8 @@ def test_kernel_name_follows_the_plan(lib):
     assert pkd.kernel_name(*args, pkd.BF16) == "chunked grid, tensor cores"
     assert pkd.kernel_name(*args, pkd.BF16, flags=pkd.FLAG_FLAT) == "persistent flat partition, tensor cores"
     assert pkd.kernel_name(8, 1, 32, 8, 128, 16, 4096, pkd.BF16) == "chunked grid, tensor cores"
-    assert pkd.kernel_name(8, 8, 32, 8, 128, 16, 4096, pkd.BF16) == "persistent flat partition, tensor cores"
+    assert pkd.kernel_name(8, 8, 32, 8, 128, 16, 4096, pkd.BF16) == "chunked grid, tensor cores"
+    assert pkd.kernel_name(8, 8, 32, 8, 128, 16, 4096, pkd.FP8_E4M3) == "persistent flat partition, tensor cores"
     assert pkd.kernel_name(*args, pkd.BF16, flags=pkd.FLAG_FMA | pkd.FLAG_GRID) == "chunked grid, CUDA cores"
     assert pkd.kernel_name(*args, pkd.FP8_E4M3) == "chunked grid, tensor cores"
     assert pkd.kernel_name(64, 8, 32, 8, 128, 16, 4096, pkd.FP8_E4M3) == "persistent flat partition, tensor cores"
