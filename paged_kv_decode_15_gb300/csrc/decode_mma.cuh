@@ -98,38 +98,31 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p
     float* wl = wm + NW * S::MROWS;
     int* flag = reinterpret_cast<int*>(smem + S::OFF_FLAG);
 
+    // Start-up in one memory round trip: the chunk's table entries (no
+    // window), the q rows and the request's length are read at once; each
+    // warp then sets up its own barriers and issues its first copies before
+    // the CTA barrier that publishes the page list and q.
+    constexpr int VPR = D * 2 / 16;  // 16-byte vectors per q row
+    constexpr int QPER = W::kCtaQ ? (S::MROWS * VPR + NW * 32 - 1) / (NW * 32) : 1;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     SpecPages<NW * 32> spec;
     spec.load(p);
-    CtaWork w;
-    if (!cta_setup<D>(p, w)) return;
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (tid == 0) {
-        prefetch_tmap(&tmap);
-        for (int i = 0; i < NW * NBUF; ++i) mbar_init(smem_u32(bars + i), 1);
-        fence_barrier_init();
-    }
-    if (spec.on)
-        spec.store(p, w, pages);
-    else
-        load_cta_pages(p, w, pages);
-
-    // stage the M query rows (zero padding rows) for ldmatrix
+    uint4 qv[QPER];
     if constexpr (W::kCtaQ) {
-        constexpr int VPR = D * 2 / 16;  // 16-byte vectors per row
         const uint4* qg = reinterpret_cast<const uint4*>(p.q);
-        for (int e = tid; e < S::MROWS * VPR; e += blockDim.x) {
-            const int r = e / VPR, v = e % VPR;
-            uint4 val = make_uint4(0u, 0u, 0u, 0u);
-            if (r < p.M) {
+        const int b = blockIdx.z, hk = blockIdx.y;
+#pragma unroll
+        for (int j = 0; j < QPER; ++j) {
+            const int e = tid + j * NW * 32, r = e / VPR, v = e % VPR;
+            qv[j] = make_uint4(0u, 0u, 0u, 0u);
+            if (e < S::MROWS * VPR && r < p.M) {
                 const int i = r / p.G, g = r % p.G;
-                const long long row = (static_cast<long long>(w.b) * p.sq + i) * p.Hq + w.hk * p.G + g;
-                val = __ldg(qg + row * VPR + v);
+                qv[j] = __ldg(qg + ((static_cast<long long>(b) * p.sq + i) * p.Hq + hk * p.G + g) * VPR + v);
             }
-            *reinterpret_cast<uint4*>(qs + r * S::QSTRIDE + v * 16) = val;
         }
     }
-    __syncthreads();
+    CtaWork w;
+    if (!cta_setup<D>(p, w)) return;
 
     const int nst = (w.t1 - w.t0 + kStageTok - 1) / kStageTok;
     const int my_n = nst > warp ? (nst - warp + NW - 1) / NW : 0;
@@ -137,9 +130,35 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p
     const uint32_t ring = smem_u32(ring_gen);
     const uint32_t bar0 = smem_u32(bars + warp * NBUF);
     const uint64_t pol = policy_evict_first();
-    if (lane == 0)
-        for (int k = 0; k < NBUF && k < my_n; ++k)
-            issue_stage<D, ELT>(&tmap, p, w, pages, warp + k * NW, ring + k * S::STAGE, bar0 + 8 * k, pol);
+    if (lane == 0) {
+        // a warp's barriers serve its own ring only
+        if (warp == 0) prefetch_tmap(&tmap);
+        for (int k = 0; k < NBUF; ++k) mbar_init(bar0 + 8 * k, 1);
+        fence_barrier_init();
+        for (int k = 0; k < NBUF && k < my_n; ++k) {
+            const int tok = w.t0 + (warp + k * NW) * kStageTok;
+            const int pg = p.block_table[static_cast<long long>(w.b) * p.bt_stride + tok / p.P];
+            const uint32_t bar = bar0 + 8 * k;
+            if (pg < 0 || pg >= p.num_pages) {  // skipped; reported when the page list is built
+                mbar_arrive(bar);
+                continue;
+            }
+            mbar_arrive_expect_tx(bar, S::STAGE);
+            tma_load_3d(ring + k * S::STAGE, &tmap, 0, (pg * p.Hkv + w.hk) * p.P + (tok % p.P), 0, bar, pol);
+        }
+    }
+    if (spec.on)
+        spec.store(p, w, pages);
+    else
+        load_cta_pages(p, w, pages);
+    if constexpr (W::kCtaQ) {
+#pragma unroll
+        for (int j = 0; j < QPER; ++j) {
+            const int e = tid + j * NW * 32, r = e / VPR, v = e % VPR;
+            if (e < S::MROWS * VPR) *reinterpret_cast<uint4*>(qs + r * S::QSTRIDE + v * 16) = qv[j];
+        }
+    }
+    __syncthreads();
 
     W wp;
     wp.setup(smem + S::OFF_SCR + warp * W::kScratchBytes);
@@ -232,6 +251,8 @@ decode_mma_pair_kernel(const __grid_constant__ CUtensorMap tmap, const DecodePar
     float* wl = wm + S::PAIRS * S::MROWS;
     int* flag = reinterpret_cast<int*>(smem + S::OFF_FLAG);
 
+    SpecPages<kNW * 32> spec;
+    spec.load(p);
     CtaWork w;
     if (!cta_setup<D>(p, w)) return;
 
@@ -245,7 +266,10 @@ decode_mma_pair_kernel(const __grid_constant__ CUtensorMap tmap, const DecodePar
         }
         fence_barrier_init();
     }
-    load_cta_pages(p, w, pages);
+    if (spec.on)
+        spec.store(p, w, pages);
+    else
+        load_cta_pages(p, w, pages);
     {
         constexpr int VPR = D * 2 / 16;
         const uint4* qg = reinterpret_cast<const uint4*>(p.q);
