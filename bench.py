@@ -155,6 +155,24 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------ device side
+def pack(torch, tensors):
+    """Copy device tensors into one allocation (views at 256-byte aligned
+    offsets), so that an end-to-end step moves all of them with one copy.
+    Returns (buffer, views)."""
+    offs, total = [], 0
+    for t in tensors:
+        offs.append(total)
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    buf = torch.empty(max(total, 256), dtype=torch.uint8, device="cuda")
+    views = []
+    for t, o in zip(tensors, offs):
+        n = t.numel() * t.element_size()
+        v = buf[o:o + n].view(t.dtype).view(t.shape)
+        v.copy_(t)
+        views.append(v)
+    return buf, views
+
+
 class PagedRunner:
     """One paged_decode call over a PagedCase, inputs resident on the device."""
     kernel = "paged decode (one launch per step)"
@@ -178,8 +196,12 @@ class PagedRunner:
                                                  case.head_dim, case.page_size, self.max_kv_len, kv_code, case.window,
                                                  self.chunk, flags), dtype=torch.uint8, device="cuda")
         pkd.workspace_init(self.ws)
-        self.inputs = [self.q, self.bt, self.lens]   # copied in every end-to-end step
-        self.outputs = [self.out, self.lse]          # copied back every end-to-end step
+        # q, table and lengths in one allocation, out and lse in another: an
+        # end-to-end step copies each pack once
+        in_buf, (self.q, self.bt, self.lens) = pack(torch, [self.q, self.bt, self.lens])
+        out_buf, (self.out, self.lse) = pack(torch, [self.out, self.lse])
+        self.inputs = [in_buf]    # copied in every end-to-end step
+        self.outputs = [out_buf]  # copied back every end-to-end step
         self.acct = algorithmic_bytes(case)
 
     def call(self):
@@ -208,7 +230,9 @@ class SegmentRunner:
         self.used = to_torch(case.used, "int32")
         self.bias = to_torch(case.bias, "fp32")
         self.out = torch.empty_like(self.q)
-        self.inputs = [self.q, self.k, self.v, self.used, self.bias]
+        in_buf, (self.q, self.k, self.v, self.used, self.bias) = pack(
+            torch, [self.q, self.k, self.v, self.used, self.bias])
+        self.inputs = [in_buf]
         self.outputs = [self.out]
         self.acct = segment_bytes(case)
 
@@ -234,7 +258,9 @@ class PagedSegmentRunner:
         self.used = to_torch(case.used, "int32")
         self.bias = to_torch(case.bias, "fp32")
         self.out = torch.empty_like(self.q)
-        self.inputs = [self.q, self.bt, self.seg_start, self.used, self.bias]
+        in_buf, (self.q, self.bt, self.seg_start, self.used, self.bias) = pack(
+            torch, [self.q, self.bt, self.seg_start, self.used, self.bias])
+        self.inputs = [in_buf]
         self.outputs = [self.out]
         Hkv, D = case.num_kv_heads, case.q.shape[2]
         kv = int(case.used.sum()) * Hkv * 2 * D * 2
@@ -260,7 +286,8 @@ class CacheWriteRunner:
         self.value = to_torch(case.value, case.in_dtype)
         self.slots = torch.from_numpy(case.slots).cuda()
         self.cache = to_torch(case.kv_cache, case.kv_dtype)
-        self.inputs = [self.key, self.value, self.slots]
+        in_buf, (self.key, self.value, self.slots) = pack(torch, [self.key, self.value, self.slots])
+        self.inputs = [in_buf]
         self.outputs = []
         live = int((case.slots >= 0).sum())
         Hkv, D = case.key.shape[1], case.key.shape[2]
@@ -549,8 +576,9 @@ def main():
             "e2e": {"value": round(job_throughput(acct["kv"], world, steps, e2e_ms), 2), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "us_per_call": round(e2e_ms / steps * 1e3, 2),
-                    "note": ("q, block_table, seq_lens in from pinned host memory, out and lse back, every step; "
-                             "the KV cache is resident device state") if isinstance(runner, PagedRunner) else
+                    "note": ("q, block_table, seq_lens in from pinned host memory (one packed copy), out and lse "
+                             "back (one packed copy), every step; the KV cache is resident device state")
+                    if isinstance(runner, PagedRunner) else
                             ("key, value, slot_mapping in from pinned host memory; the cache is resident "
                              "device state") if isinstance(runner, CacheWriteRunner) else
                             ("q, block_table, seg_start, used, bias in, out back; the cache is resident device "
