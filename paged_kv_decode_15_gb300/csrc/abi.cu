@@ -234,13 +234,16 @@ pkd_status get_map(CUtensorMap& out, const void* base, int rank, uint64_t d0, ui
 
 // The "stage map" of a paged cache: {128-byte chunk, key row, chunk of the
 // row}, strides {row bytes, 128 B}, box {one chunk, 16 rows, every chunk},
-// so one TMA copy loads a 16-key stage (K and V) chunk-major.
-pkd_status get_stage_map(CUtensorMap& out, const void* cache, uint64_t rows, int row_bytes, pkd_dtype dt) {
+// so one TMA copy loads a 16-key stage (K and V) chunk-major.  With
+// half_rows the box is {one chunk, 8 rows, one chunk}: one copy per chunk
+// fills the first 8 rows of that chunk's 16-row slot.
+pkd_status get_stage_map(CUtensorMap& out, const void* cache, uint64_t rows, int row_bytes, pkd_dtype dt,
+                         bool half_rows = false) {
     const int elt = elt_bytes(dt);
     MapKey k;
     std::memset(&k, 0, sizeof k);
     k.base = cache; k.d0 = 128 / elt; k.d1 = rows; k.d2 = row_bytes / 128; k.s1 = row_bytes; k.s2 = 128;
-    k.rank = 103; k.dtype = dt;
+    k.rank = half_rows ? 108 : 103; k.dtype = dt;
     MapCache& c = map_cache();
     {
         std::lock_guard<std::mutex> g(c.mu);
@@ -257,7 +260,8 @@ pkd_status get_stage_map(CUtensorMap& out, const void* cache, uint64_t rows, int
                                                    : CU_TENSOR_MAP_DATA_TYPE_UINT8;
     cuuint64_t dims[3] = {k.d0, k.d1, k.d2};
     cuuint64_t strides[2] = {k.s1, k.s2};
-    cuuint32_t box[3] = {(cuuint32_t)(128 / elt), (cuuint32_t)pkd::kStageTok, (cuuint32_t)(row_bytes / 128)};
+    cuuint32_t box[3] = {(cuuint32_t)(128 / elt), (cuuint32_t)(half_rows ? pkd::kStageTok / 2 : pkd::kStageTok),
+                         (cuuint32_t)(half_rows ? 1 : row_bytes / 128)};
     cuuint32_t estr[3] = {1, 1, 1};
     CUtensorMap m;
     CUresult r = enc(&m, t, 3, const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -548,7 +552,8 @@ pkd_status pkd_segmented_attention_paged(const void* q, pkd_dtype dtype, const v
     const uint64_t rows = (uint64_t)num_pages * num_kv_heads * page_size;
     pkd_status st = get_stage_map(p.kmap, kv_cache, rows, 4 * head_dim, dtype);
     if (st != PKD_OK) return st;
-    p.vmap = p.kmap;
+    st = get_stage_map(p.vmap, kv_cache, rows, 4 * head_dim, dtype, true);  // stages whose keys end in 8 rows
+    if (st != PKD_OK) return st;
     p.paged = 1;
     p.block_table = block_table;
     p.bt_stride = block_table_stride;

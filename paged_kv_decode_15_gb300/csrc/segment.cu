@@ -190,6 +190,14 @@ segmented_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             }
             const int tok0 = sa[g] + sidx * kStageTok;
             const int crow = (pg * p.Hkv + hk) * p.P + tok0 % p.P;
+            if (ss[g] + su[g] - tok0 <= kStageTok / 2) {
+                // the segment ends in the stage's first 8 rows: load only those
+                // (rows 8..15 are masked and their V rows zeroed before use)
+                mbar_arrive_expect_tx(bar, S::STAGE / 2);
+#pragma unroll
+                for (int c = 0; c < D * 4 / 128; ++c) tma_load_3d(buf + c * 2048, &vmap, 0, crow, c, bar, pol);
+                return;
+            }
             mbar_arrive_expect_tx(bar, S::STAGE);
             tma_load_3d(buf, &kmap, 0, crow, 0, bar, pol);
             return;

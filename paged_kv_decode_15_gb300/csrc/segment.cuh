@@ -9,6 +9,7 @@ namespace pkd {
 struct SegmentParams {
     CUtensorMap kmap, vmap;   // 3-D maps over k, v: {head_dim, Hkv, rows}; paged: kmap is the
                               // cache's stage map {128-byte chunk, pages*Hkv*P rows, chunks}
+                              // and vmap the same map with 8-row, one-chunk boxes
     const int32_t* block_table;  // paged: [n, bt_stride]
     const int32_t* seg_start;    // paged: [n, topk+1] first key position of each segment
     long long bt_stride, num_pages;

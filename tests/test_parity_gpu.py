@@ -61,6 +61,9 @@ SMALL = {
     "bf16_causal_sq4_m16": (dict(seq_lens=LENS, sq=4, causal=True), dict(chunk_tokens=64)),
     "bf16_causal_sq4_window50": (dict(seq_lens=LENS, sq=4, causal=True, window=50), dict(chunk_tokens=32)),
     "bf16_causal_sq2_g2": (dict(seq_lens=LENS, sq=2, num_heads=4, num_kv_heads=2, causal=True, window=30), dict()),
+    "bf16_causal_sq8_m32_window": (dict(seq_lens=LENS, sq=8, causal=True, window=200), dict(chunk_tokens=64)),
+    "bf16_causal_sq8_m32_auto": (dict(seq_lens=LENS, sq=8, causal=True), dict()),
+    "fp16_sq6_g4_m24_p32": (dict(seq_lens=LENS, sq=6, dtype="fp16", page_size=32), dict(chunk_tokens=96)),
     "fp8_g8": (dict(seq_lens=LENS, dtype="fp8", num_heads=64, num_kv_heads=8), dict(chunk_tokens=64)),
     "fp8_g4_p64": (dict(seq_lens=LENS, dtype="fp8", page_size=64), dict()),
     "fp8_g2_window": (dict(seq_lens=LENS, dtype="fp8", num_heads=16, num_kv_heads=8, window=100), dict()),
