@@ -45,7 +45,7 @@ typedef enum {
 
 /* Flags for pkd_paged_decode. */
 #define PKD_FLAG_CAUSAL 1u      /* causal mask inside the query block, exact per-token window */
-#define PKD_FLAG_MMA_SMALL_M 2u /* tensor cores for sq*Hq/Hkv < 16 (the default for 16-bit caches) */
+#define PKD_FLAG_MMA_SMALL_M 2u /* tensor cores for sq*Hq/Hkv < 16 (already the default; kept for callers) */
 #define PKD_FLAG_FMA 4u         /* CUDA cores instead (only when sq*Hq/Hkv <= 8) */
 #define PKD_FLAG_GRID 8u        /* the chunked grid: one CTA per Split-KV chunk */
 #define PKD_FLAG_FLAT 16u       /* the persistent flat partition whatever the shapes (batch <= 1024) */
