@@ -8,8 +8,11 @@ epilogue, all in one kernel launch).  Inputs are resident in HBM; the L2 is
 flushed before every timed step (a 512 MiB write, then a 256 MiB read so that
 no dirty line of the flush is written back inside the step; --l2-flush write
 keeps only the write) and the KV stream is larger than the L2 anyway.  Each step is timed with CUDA events on the launching
-stream; value = algorithmic KV bytes of all ranks / max over ranks of the
-summed step time.  One JSON line is printed by rank 0.
+stream, around a direct call (--graph replays one captured call instead, so
+that host-side launch overhead cannot open gaps inside a step).  value =
+algorithmic KV bytes of all ranks / max over ranks of the summed step time.
+One JSON line is printed by rank 0.  The end-to-end figure (e2e) always goes
+through the direct call.
 
 --impl reference times the fp64 CPU oracle on the host cores instead, on a
 bounded sample of the same workload per step, in the same metric.
@@ -346,6 +349,26 @@ def run_gpu(args, rank, world, dist):
     torch.cuda.synchronize()
     runner.check()
 
+    # With --graph the timed steps replay one captured call, so that the
+    # host's launch overhead (the binding's argument checks, ctypes) cannot
+    # open gaps between a step's events even when the host falls behind the
+    # GPU; the kernel and its arguments are those of the direct call.
+    step_call, launch_mode = runner.call, "direct"
+    if args.graph:
+        try:
+            side = torch.cuda.Stream()
+            side.wait_stream(stream)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(side):
+                with torch.cuda.graph(graph, stream=side):
+                    runner.call()
+            stream.wait_stream(side)
+            torch.cuda.synchronize()
+            step_call, launch_mode = graph.replay, "CUDA graph of one call, replayed every step"
+        except RuntimeError as e:  # capture refused: time direct calls and say so
+            launch_mode = f"direct (graph capture failed: {e})"
+    args.launch_mode = launch_mode
+
     sampler = ClockSampler(torch.cuda.current_device())
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -356,7 +379,7 @@ def run_gpu(args, rank, world, dist):
     for i in range(args.steps):
         flush.zero_()
         starts[i].record(stream)
-        runner.call()
+        step_call()
         ends[i].record(stream)
     torch.cuda.synchronize()
     t1 = time.time()
@@ -539,6 +562,8 @@ def main():
     ap.add_argument("--grid", action="store_true", help="force the chunked grid (one CTA per Split-KV chunk)")
     ap.add_argument("--flat", action="store_true", help="force the persistent flat partition")
     ap.add_argument("--balanced", action="store_true", help="force the persistent per-CTA partition")
+    ap.add_argument("--graph", action="store_true",
+                    help="time replays of one captured call instead of direct calls")
     ap.add_argument("--l2-flush", default="write-read", choices=["write", "write-read"],
                     help="how L2 is evicted before every timed step: a 512 MiB write (it leaves up to an L2 of "
                          "dirty lines whose write-back lands inside the timed step), or that write followed by a "
@@ -592,6 +617,7 @@ def main():
                              "state") if isinstance(runner, PagedSegmentRunner) else
                             "q, k, v, used, bias in from pinned host memory and out back, every step"},
             "gpu_launches": steps,
+            "launch": getattr(args, "launch_mode", "direct"),
             "clocks": clocks,
         }
         if not args.no_cpu_baseline and isinstance(runner, PagedRunner):
