@@ -125,11 +125,7 @@ decode_flat_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams 
     const int b_begin = tid * per, b_end = min(B, b_begin + per);
     int local = 0;
     for (int b = b_begin; b < b_end; ++b) {
-        int L = p.seq_lens[b];
-        if (L < 0 || L > p.max_kv_len) {
-            if (blockIdx.x == 0) raise_status(p, kErrBounds);
-            L = L < 0 ? 0 : p.max_kv_len;
-        }
+        const int L = clamp_len(p, b, blockIdx.x == 0);
         lens[b] = L;
         const int vis = L - visible_lo(p, L);
         local += (vis + kStageTok - 1) / kStageTok;
@@ -157,17 +153,8 @@ decode_flat_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams 
     const long long Stot = static_cast<long long>(pre[B]) * Hkv;
 
     // ---- requests with no visible key: out = 0, lse = -inf
-    for (int b = blockIdx.x; b < B; b += gridDim.x) {
-        if (pre[b + 1] != pre[b]) continue;
-        for (int e = tid; e < p.Hkv * p.M * D; e += blockDim.x) {
-            const int hk = e / (p.M * D), r = (e / D) % p.M, d = e % D;
-            store_out(p.out, out_index(p, b, hk, r, d, D), 0.f, p.out_dtype);
-            if (d == 0 && p.lse) {
-                const int i = r / p.G, g = r % p.G;
-                p.lse[(static_cast<long long>(b) * p.sq + i) * p.Hq + hk * p.G + g] = -INFINITY;
-            }
-        }
-    }
+    for (int b = blockIdx.x; b < B; b += gridDim.x)
+        if (pre[b + 1] == pre[b]) write_empty_request<D>(p, b);
 
     // ---- this warp's slice of the flat stage sequence
     static_assert(kNW % RT == 0, "row-tile groups must not straddle CTAs");

@@ -27,14 +27,6 @@ static cudaError_t launch_one(const CUtensorMap& tmap, const DecodeParams& p, di
     X(64, 0, 8, 2) X(64, 0, 8, 4) X(64, 0, 16, 8)                             \
     X(64, 1, 8, 2) X(64, 1, 8, 4) X(64, 1, 16, 8)
 
-int decode_fma_smem(int D, int kvt, int LPT, int MR) {
-#define PKD_FMA_SMEM(d, k, l, m) \
-    if (D == d && kvt == k && LPT == l && MR == m) return FmaShape<d, k, l, m, kFmaNbuf>::SMEM;
-    PKD_FMA_VARIANTS(PKD_FMA_SMEM)
-#undef PKD_FMA_SMEM
-    return -1;
-}
-
 cudaError_t launch_decode_fma(int D, int kvt, int LPT, int MR, const CUtensorMap& tmap,
                               const DecodeParams& p, dim3 grid, cudaStream_t stream) {
 #define PKD_FMA_CASE(d, k, l, m) \

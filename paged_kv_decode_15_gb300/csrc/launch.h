@@ -10,10 +10,6 @@ namespace pkd {
 
 struct DecodeParams;
 
-// Dynamic shared memory of a decode kernel variant (bytes), or -1 if the
-// variant is not built.
-int decode_fma_smem(int D, int kvt, int LPT, int MR);
-
 // Launch one decode kernel variant on `stream`; grid = (max_splits, Hkv, B).
 cudaError_t launch_decode_mma(int D, bool bf16, int MT, int NT, const CUtensorMap& tmap,
                               const DecodeParams& p, dim3 grid, cudaStream_t stream);
