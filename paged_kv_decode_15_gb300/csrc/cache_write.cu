@@ -22,15 +22,9 @@ struct CacheWriteParams {
     uint8_t* cache;         // [num_pages, Hkv, P, 2D]
     long long T, key_stride, value_stride, num_slots;  // num_slots = num_pages * P
     int Hkv, D, P, kv_elt, in_bf16;
-    int dshift;             // log2(D / 8): 16-byte input chunks per head row
     float k_scale, v_scale;
     float k_inv, v_inv;     // 1/scale when that scale is a power of two (then x*inv == x/scale exactly), else 0
 };
-
-// x / scale rounded to nearest: a multiply when the reciprocal is exact
-__device__ __forceinline__ float scaled(float x, float scale, float inv) {
-    return inv != 0.f ? x * inv : __fdiv_rn(x, scale);
-}
 
 __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
     uint16_t r;
@@ -40,21 +34,26 @@ __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
 
 constexpr int kChunksPerLane = 8;  // loads in flight per lane (a token of 8 heads x 128: all of it)
 
+// D, the cache type, the input type and the division mode are template
+// parameters so that the per-chunk work has no runtime branches.
+template <int D, bool kFp8, bool kBF16In, bool kExactInv>
 __global__ void __launch_bounds__(128) cache_write_kernel(const CacheWriteParams p) {
+    constexpr int kDShift = D == 128 ? 4 : 3;  // log2 of the 16-byte input chunks per head row
+    constexpr int kEltOut = kFp8 ? 1 : 2;
     const long long t = static_cast<long long>(blockIdx.x) * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (t >= p.T) return;
     const long long s = __ldg(p.slots + t);
     if (s < 0 || s >= p.num_slots) return;  // padding (negative) or outside the cache: nothing written
     const int page = static_cast<int>(s / p.P), off = static_cast<int>(s % p.P);
-    const int per_part = p.Hkv << p.dshift;  // 16-byte input chunks of the key rows (and of the value rows)
+    const int per_part = p.Hkv << kDShift;  // 16-byte input chunks of the key rows (and of the value rows)
     const int total = 2 * per_part;
-    const int dmask = (1 << p.dshift) - 1;
+    constexpr int dmask = (1 << kDShift) - 1;
     const uint8_t* krow = p.key + t * p.key_stride * 2;
     const uint8_t* vrow = p.value + t * p.value_stride * 2;
     // cache row of (page, head 0, off): heads are P rows apart
-    uint8_t* dst0 = p.cache + ((static_cast<long long>(page) * p.Hkv * p.P + off) * 2 * p.D) * p.kv_elt;
-    const long long head_stride = static_cast<long long>(p.P) * 2 * p.D * p.kv_elt;
+    uint8_t* dst0 = p.cache + ((static_cast<long long>(page) * p.Hkv * p.P + off) * 2 * D) * kEltOut;
+    const long long head_stride = static_cast<long long>(p.P) * 2 * D * kEltOut;
 
     for (int base = 0; base < total; base += 32 * kChunksPerLane) {
         uint4 v[kChunksPerLane];
@@ -71,30 +70,30 @@ __global__ void __launch_bounds__(128) cache_write_kernel(const CacheWriteParams
             const int c = base + i * 32 + lane;
             if (c >= total) continue;
             const int part = c >= per_part, j = c - part * per_part;
-            const int h = j >> p.dshift, e = (j & dmask) * 8;  // head, first element of the chunk
-            uint8_t* dst = dst0 + h * head_stride + (part * p.D + e) * p.kv_elt;
-            if (p.kv_elt == 2) {
+            const int h = j >> kDShift, e = (j & dmask) * 8;  // head, first element of the chunk
+            uint8_t* dst = dst0 + h * head_stride + (part * D + e) * kEltOut;
+            if constexpr (!kFp8) {
                 *reinterpret_cast<uint4*>(dst) = v[i];
-                continue;
-            }
-            const float scale = part ? p.v_scale : p.k_scale;
-            const float inv = part ? p.v_inv : p.k_inv;
-            const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-            uint32_t out[2];
+            } else {
+                const float scale = part ? p.v_scale : p.k_scale;
+                const float inv = part ? p.v_inv : p.k_inv;
+                auto q8 = [&](float x) { return kExactInv ? x * inv : __fdiv_rn(x, scale); };
+                const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+                uint32_t out[2];
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                float f[4];
-                if (p.in_bf16) {
-                    bf16x2_to_f32(w[2 * q], f[0], f[1]);
-                    bf16x2_to_f32(w[2 * q + 1], f[2], f[3]);
-                } else {
-                    f16x2_to_f32(w[2 * q], f[0], f[1]);
-                    f16x2_to_f32(w[2 * q + 1], f[2], f[3]);
+                for (int q = 0; q < 2; ++q) {
+                    float f[4];
+                    if constexpr (kBF16In) {
+                        bf16x2_to_f32(w[2 * q], f[0], f[1]);
+                        bf16x2_to_f32(w[2 * q + 1], f[2], f[3]);
+                    } else {
+                        f16x2_to_f32(w[2 * q], f[0], f[1]);
+                        f16x2_to_f32(w[2 * q + 1], f[2], f[3]);
+                    }
+                    out[q] = f32x2_to_e4m3x2(q8(f[0]), q8(f[1])) | (f32x2_to_e4m3x2(q8(f[2]), q8(f[3])) << 16);
                 }
-                out[q] = f32x2_to_e4m3x2(scaled(f[0], scale, inv), scaled(f[1], scale, inv)) |
-                         (f32x2_to_e4m3x2(scaled(f[2], scale, inv), scaled(f[3], scale, inv)) << 16);
+                *reinterpret_cast<uint2*>(dst) = make_uint2(out[0], out[1]);
             }
-            *reinterpret_cast<uint2*>(dst) = make_uint2(out[0], out[1]);
         }
     }
 }
@@ -115,7 +114,6 @@ cudaError_t launch_cache_write(const void* key, const void* value, int in_dtype,
     p.Hkv = Hkv;
     p.D = D;
     p.P = P;
-    p.dshift = D == 128 ? 4 : 3;
     p.kv_elt = kv_dtype == 2 ? 1 : 2;
     p.in_bf16 = in_dtype == 0;
     p.k_scale = k_scale;
@@ -129,7 +127,15 @@ cudaError_t launch_cache_write(const void* key, const void* value, int in_dtype,
     p.k_inv = exact_inv(k_scale);
     p.v_inv = exact_inv(v_scale);
     if (T == 0) return cudaSuccess;
-    cache_write_kernel<<<static_cast<unsigned>((T + 3) / 4), 128, 0, stream>>>(p);
+    const dim3 grid(static_cast<unsigned>((T + 3) / 4));
+    const bool fp8 = p.kv_elt == 1, exact = p.k_inv != 0.f && p.v_inv != 0.f;
+#define PKD_CW(d, f8, bf, ex) \
+    if (D == d && fp8 == f8 && (f8 ? (p.in_bf16 != 0) == bf && exact == ex : !bf && !ex)) \
+        cache_write_kernel<d, f8, bf, ex><<<grid, 128, 0, stream>>>(p);
+    PKD_CW(128, false, false, false) PKD_CW(64, false, false, false)
+    PKD_CW(128, true, true, true) PKD_CW(128, true, true, false) PKD_CW(128, true, false, true) PKD_CW(128, true, false, false)
+    PKD_CW(64, true, true, true) PKD_CW(64, true, true, false) PKD_CW(64, true, false, true) PKD_CW(64, true, false, false)
+#undef PKD_CW
     return cudaGetLastError();
 }
 
