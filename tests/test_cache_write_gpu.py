@@ -55,6 +55,21 @@ def test_cache_write_is_bit_exact(in_dt, kv_dt, D, P):
     assert np.array_equal(got.view(ref.dtype), ref)
 
 
+@pytest.mark.parametrize("in_dt,D,P,ks,vs", [("bf16", 128, 16, 0.0137, 0.021), ("fp16", 64, 32, 0.0091, 1.0 / 64)])
+def test_cache_write_fp8_scales_that_are_not_powers_of_two(in_dt, D, P, ks, vs):
+    """The quotient then takes an IEEE division on both sides (no exact reciprocal)."""
+    import paged_kv_decode_15_gb300 as pkd
+    T, Hkv, num_pages = 257, 2, 40
+    key, value, slots, cache = _case(T, Hkv, D, P, num_pages, in_dt, "fp8", seed=D + P + 7)
+    ref = oracle.cache_write(key, value, in_dt, slots, cache, "fp8", num_kv_heads=Hkv, head_dim=D, page_size=P,
+                             k_scale=ks, v_scale=vs)
+    dev_cache = gu.to_dev(cache, "fp8")
+    pkd.cache_write(gu.to_dev(key, in_dt), gu.to_dev(value, in_dt), torch.from_numpy(slots).cuda(), dev_cache,
+                    k_scale=ks, v_scale=vs)
+    torch.cuda.synchronize()
+    assert np.array_equal(dev_cache.cpu().numpy().view(np.uint8), ref.view(np.uint8))
+
+
 def test_cache_write_strided_rows():
     """key/value as slices of a fused [T, 3, Hkv, D] projection output."""
     import paged_kv_decode_15_gb300 as pkd

@@ -248,3 +248,11 @@ def test_long_slices_reload_the_page_list(sq):
     case = wl.paged_case(name="long", seq_lens=[2_000_000], sq=sq, num_heads=4, num_kv_heads=1, head_dim=64,
                          pool_factor=1.0, seed=31 + sq)
     _check(case, balanced=True)
+
+
+@pytest.mark.parametrize("dtype,sq", [("fp8", 1), ("bf16", 8)])
+def test_batch_above_the_flat_table_limit(dtype, sq):
+    """1500 short requests: the chunked grid (e4m3 warp, or warp pairs for 32 rows)."""
+    lens = np.random.default_rng(77).integers(0, 70, size=1500).astype(np.int32)
+    case = wl.paged_case(name="wide", seq_lens=lens, sq=sq, dtype=dtype, seed=78)
+    _check(case, batch_index=list(range(0, 1500, 97)))
