@@ -404,6 +404,15 @@ pkd_status pkd_paged_decode(const void* q, pkd_dtype q_dtype, const void* kv_cac
     p.window = window > 0 ? window : 0;
     p.causal = (flags & PKD_FLAG_CAUSAL) ? 1 : 0;
     p.out_dtype = (int)out_dtype;
+    {
+        // magic number for tok / page_size (0 <= tok < 2^31): with l = ceil(log2 P),
+        // m = floor(2^(31+l) / P) + 1 (2^31 for a power of two) and shift 31 + l
+        int l = 0;
+        while ((1 << l) < page_size) ++l;
+        const bool pow2 = (page_size & (page_size - 1)) == 0;
+        p.pmagic = pow2 ? 0x80000000u : (uint32_t)(((uint64_t)1 << (31 + l)) / (uint64_t)page_size + 1);
+        p.pmshift = 31 + l;
+    }
     p.scale_log2 = scale * q_scale * k_scale * pkd::kLog2e;
     p.v_scale = v_scale;
 

@@ -31,6 +31,8 @@ struct DecodeParams {
     int B, sq, Hq, Hkv, G, M, P;
     int max_kv_len, chunk, max_splits, window, causal;
     int out_dtype;               // 0 bf16, 1 fp16, 3 fp32
+    uint32_t pmagic;             // tok / P == (tok * pmagic) >> pmshift for 0 <= tok < 2^31
+    int pmshift;
     float scale_log2;            // scale * q_scale * k_scale * log2(e)
     float v_scale;
 };
@@ -157,6 +159,14 @@ __device__ __forceinline__ bool row_sees(const DecodeParams& p, int L, int row, 
     return p.window <= 0 || tok >= pos - (p.window - 1);
 }
 
+// Table column and slot of key `tok` without a division: a 32x32->64-bit
+// multiply by a magic number and a shift (division by an invariant integer,
+// Granlund and Montgomery, exact for every dividend below 2^31).
+__device__ __forceinline__ int page_col(const DecodeParams& p, int tok) {
+    return static_cast<int>((static_cast<unsigned long long>(static_cast<uint32_t>(tok)) * p.pmagic) >> p.pmshift);
+}
+__device__ __forceinline__ int page_slot(const DecodeParams& p, int tok) { return tok - page_col(p, tok) * p.P; }
+
 // Load the page indices of this CTA's keys [t0, t1) into shared memory
 // (pages[i] holds table column t0/P + i; t0 need not be page-aligned); a page
 // outside [0, num_pages) becomes -1 (its keys are skipped) and raises the
@@ -176,7 +186,7 @@ __device__ __forceinline__ void load_cta_pages(const DecodeParams& p, const CtaW
 
 // Page of key `tok` (in [t0, t1)) from the list load_cta_pages made.
 __device__ __forceinline__ int page_of(const DecodeParams& p, const CtaWork& w, const int* pages, int tok) {
-    return pages[tok / p.P - w.t0 / p.P];
+    return pages[page_col(p, tok) - page_col(p, w.t0)];
 }
 
 // Issue the TMA load of one 16-key stage.  The stage map views the cache as
@@ -196,7 +206,7 @@ __device__ __forceinline__ void issue_stage(const CUtensorMap* tmap, const Decod
         mbar_arrive(bar);
         return;
     }
-    const int row = (pg * p.Hkv + w.hk) * p.P + (tok % p.P);
+    const int row = (pg * p.Hkv + w.hk) * p.P + page_slot(p, tok);
     mbar_arrive_expect_tx(bar, 2 * HALF);
     tma_load_3d(buf, tmap, 0, row, 0, bar, policy);  // the whole 16-key stage in one copy
 }

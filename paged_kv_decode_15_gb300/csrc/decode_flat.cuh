@@ -189,7 +189,7 @@ decode_flat_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams 
             m.hk = static_cast<int>(loc / cnt);
             m.s = static_cast<int>(loc % cnt);
             const int tok = visible_lo(p, lens[b]) + m.s * kStageTok;
-            int pg = p.block_table[static_cast<long long>(b) * p.bt_stride + tok / p.P];
+            int pg = p.block_table[static_cast<long long>(b) * p.bt_stride + page_col(p, tok)];
             if (pg < 0 || pg >= p.num_pages) {
                 raise_status(p, kErrBounds);
                 pg = -1;
@@ -220,7 +220,7 @@ decode_flat_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams 
             return;
         }
         const int tok = visible_lo(p, lens[m.b]) + m.s * kStageTok;
-        const int row = (m.page * p.Hkv + m.hk) * p.P + (tok % p.P);
+        const int row = (m.page * p.Hkv + m.hk) * p.P + page_slot(p, tok);
         mbar_arrive_expect_tx(bar, S::STAGE);
         tma_load_3d(buf, &tmap, 0, row, 0, bar, pol);
     };

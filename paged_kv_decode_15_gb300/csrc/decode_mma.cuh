@@ -137,14 +137,14 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p
         fence_barrier_init();
         for (int k = 0; k < NBUF && k < my_n; ++k) {
             const int tok = w.t0 + (warp + k * NW) * kStageTok;
-            const int pg = p.block_table[static_cast<long long>(w.b) * p.bt_stride + tok / p.P];
+            const int pg = p.block_table[static_cast<long long>(w.b) * p.bt_stride + page_col(p, tok)];
             const uint32_t bar = bar0 + 8 * k;
             if (pg < 0 || pg >= p.num_pages) {  // skipped; reported when the page list is built
                 mbar_arrive(bar);
                 continue;
             }
             mbar_arrive_expect_tx(bar, S::STAGE);
-            tma_load_3d(ring + k * S::STAGE, &tmap, 0, (pg * p.Hkv + w.hk) * p.P + (tok % p.P), 0, bar, pol);
+            tma_load_3d(ring + k * S::STAGE, &tmap, 0, (pg * p.Hkv + w.hk) * p.P + page_slot(p, tok), 0, bar, pol);
         }
     }
     if (spec.on)
