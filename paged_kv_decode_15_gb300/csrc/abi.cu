@@ -152,6 +152,18 @@ pkd_status make_plan(int B, int sq, int Hq, int Hkv, int D, int P, int max_kv_le
     return PKD_OK;
 }
 
+// Magic number for tok / P (0 <= tok < 2^31, 1 <= P < 2^31), division by an
+// invariant integer after Granlund and Montgomery: with l = ceil(log2 P),
+// m = floor(2^(31+l) / P) + 1 (2^31 when P is a power of two) and the shift
+// 31 + l, tok / P == (tok * m) >> (31 + l).
+void page_magic(int P, uint32_t& magic, int& shift) {
+    int l = 0;
+    while ((1LL << l) < P) ++l;
+    const bool pow2 = (P & (P - 1)) == 0;
+    magic = pow2 ? 0x80000000u : (uint32_t)(((uint64_t)1 << (31 + l)) / (uint64_t)P + 1);
+    shift = 31 + l;
+}
+
 // ---------------------------------------------------------- TMA descriptors
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -404,15 +416,7 @@ pkd_status pkd_paged_decode(const void* q, pkd_dtype q_dtype, const void* kv_cac
     p.window = window > 0 ? window : 0;
     p.causal = (flags & PKD_FLAG_CAUSAL) ? 1 : 0;
     p.out_dtype = (int)out_dtype;
-    {
-        // magic number for tok / page_size (0 <= tok < 2^31): with l = ceil(log2 P),
-        // m = floor(2^(31+l) / P) + 1 (2^31 for a power of two) and shift 31 + l
-        int l = 0;
-        while ((1 << l) < page_size) ++l;
-        const bool pow2 = (page_size & (page_size - 1)) == 0;
-        p.pmagic = pow2 ? 0x80000000u : (uint32_t)(((uint64_t)1 << (31 + l)) / (uint64_t)page_size + 1);
-        p.pmshift = 31 + l;
-    }
+    page_magic(page_size, p.pmagic, p.pmshift);
     p.scale_log2 = scale * q_scale * k_scale * pkd::kLog2e;
     p.v_scale = v_scale;
 
@@ -564,6 +568,7 @@ pkd_status pkd_segmented_attention_paged(const void* q, pkd_dtype dtype, const v
     st = get_stage_map(p.vmap, kv_cache, rows, 4 * head_dim, dtype, true);  // stages whose keys end in 8 rows
     if (st != PKD_OK) return st;
     p.paged = 1;
+    page_magic(page_size, p.pmagic, p.pmshift);
     p.block_table = block_table;
     p.bt_stride = block_table_stride;
     p.seg_start = seg_start;

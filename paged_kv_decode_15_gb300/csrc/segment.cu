@@ -39,6 +39,11 @@ struct SegShape {
     static constexpr int SMEM = OFF_PAGE + kMaxSegStages * 4 + 1024;
 };
 
+// tok / P by a magic-number multiply (exact for 0 <= tok < 2^31)
+__device__ __forceinline__ int seg_page_col(const SegmentParams& p, int tok) {
+    return static_cast<int>((static_cast<unsigned long long>(static_cast<uint32_t>(tok)) * p.pmagic) >> p.pmshift);
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
     for (int m = 16; m >= 1; m >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, m));
@@ -128,7 +133,7 @@ segmented_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             int g = 0;
             while (g + 1 < groups && pre[g + 1] <= s2) ++g;
             const int tok0 = sa[g] + (s2 - pre[g]) * kStageTok;
-            int pg = p.block_table[static_cast<long long>(i) * p.bt_stride + tok0 / p.P];
+            int pg = p.block_table[static_cast<long long>(i) * p.bt_stride + seg_page_col(p, tok0)];
             spage[s2] = (pg < 0 || pg >= p.num_pages) ? -1 : pg;
         }
         __syncthreads();
@@ -189,7 +194,7 @@ segmented_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                 return;
             }
             const int tok0 = sa[g] + sidx * kStageTok;
-            const int crow = (pg * p.Hkv + hk) * p.P + tok0 % p.P;
+            const int crow = (pg * p.Hkv + hk) * p.P + (tok0 - seg_page_col(p, tok0) * p.P);
             if (ss[g] + su[g] - tok0 <= kStageTok / 2) {
                 // the segment ends in the stage's first 8 rows: load only those
                 // (rows 8..15 are masked and their V rows zeroed before use)

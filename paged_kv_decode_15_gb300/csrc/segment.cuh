@@ -14,6 +14,8 @@ struct SegmentParams {
     const int32_t* seg_start;    // paged: [n, topk+1] first key position of each segment
     long long bt_stride, num_pages;
     int P, max_kv_len, paged;
+    uint32_t pmagic;          // paged: tok / P == (tok * pmagic) >> pmshift for 0 <= tok < 2^31
+    int pmshift;
     const void* q;            // [n, Hq, D]
     const int32_t* used;      // [n, topk+1]
     const float* bias;        // [n, topk]
