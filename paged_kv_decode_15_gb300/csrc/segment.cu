@@ -141,24 +141,29 @@ segmented_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
 
     // stage list of this warp: fused mode takes stages round-robin over the
     // union; segment-output mode takes whole segments g = warp, warp + 4, ...
-    auto stage_of = [&](int k, int& g, int& sidx) {
+    // A cursor per walk (the copies issued ahead, the stages consumed) that
+    // only moves forward: fused mode tracks the group of stage s (the union's
+    // stages in order); segment-output mode the warp's current group and how
+    // many of the warp's stages precede it.
+    struct StageCursor {
+        int g, before;
+    };
+    auto stage_of = [&](StageCursor& c, int k, int& g, int& sidx) {
         if constexpr (!kSegOut) {
             const int s = warp + k * kNW;
-            g = 0;
-            while (g + 1 < groups && pre[g + 1] <= s) ++g;
+            while (c.g + 1 < groups && pre[c.g + 1] <= s) ++c.g;
+            g = c.g;
             sidx = s - pre[g];
         } else {
-            g = warp;
-            int rem = k;
-            while (g < groups) {
-                const int ns = pre[g + 1] - pre[g];
-                if (rem < ns) break;
-                rem -= ns;
-                g += kNW;
+            while (c.g < groups && k - c.before >= pre[c.g + 1] - pre[c.g]) {
+                c.before += pre[c.g + 1] - pre[c.g];
+                c.g += kNW;
             }
-            sidx = rem;
+            g = c.g;
+            sidx = k - c.before;
         }
     };
+    StageCursor issue_cur{kSegOut ? warp : 0, 0}, use_cur{kSegOut ? warp : 0, 0};
     int my_n = 0;
     if constexpr (!kSegOut) {
         const int total = pre[groups];
@@ -184,7 +189,7 @@ segmented_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     const uint64_t pol = policy_evict_first();
     auto issue = [&](int k) {
         int g, sidx;
-        stage_of(k, g, sidx);
+        stage_of(issue_cur, k, g, sidx);
         const uint32_t buf = ring + (k % kSegNbuf) * S::STAGE;
         const uint32_t bar = bar0 + 8 * (k % kSegNbuf);
         if constexpr (kPaged) {
@@ -270,7 +275,7 @@ segmented_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         }
         consumed = k + 1;
         int g, sidx;
-        stage_of(k, g, sidx);
+        stage_of(use_cur, k, g, sidx);
         // keys [lo, nvalid) of this stage belong to the segment
         int nvalid, lo = 0;
         if constexpr (kPaged) {
