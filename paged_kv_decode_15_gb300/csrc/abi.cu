@@ -44,6 +44,11 @@ int elt_bytes(pkd_dtype dt) { return dt == PKD_FP8_E4M3 ? 1 : dt == PKD_FP32 ? 4
 // gqa_decode_b64 (M = 4) 2048 (1024-key chunks) beats 512- to 2048-key chunks.
 constexpr int kTargetCtas = 2048;
 constexpr int kMaxChunk = 4096;    // and never puts more keys than this in one chunk
+// The e4m3 grid kernel holds four CTAs on each of GB300's 152 SMs; its chunks
+// fill at most two such waves (fp8_long_b8, 64 units of 131,072 keys: 19
+// chunks of 6912 keys, 1216 CTAs, 408 us against 429 us with 32 chunks of
+// 4096 and 423 us with 16 of 8192, whose second wave is two-thirds full).
+constexpr int kFp8WaveCtas = 4 * 152;
 constexpr size_t kHeader = 256;    // workspace status word lives in the first bytes
 
 struct Plan {
@@ -74,8 +79,8 @@ pkd_status make_plan(int B, int sq, int Hq, int Hkv, int D, int P, int max_kv_le
     const int M = pl.M;
     // Kernel choice (measured): the chunked grid, whose hardware CTA
     // scheduling keeps every SM busy to the end (gqa_decode_b64: 101 us
-    // against 124 us per-warp and 115 us per-CTA partitions; fp8_long_b8: 482
-    // against 489 us; query_block_sq8 with warp pairs: 193 against 214 us;
+    // against 124 us per-warp and 115 us per-CTA partitions; fp8_long_b8: 408
+    // against 476 us; query_block_sq8 with warp pairs: 193 against 214 us;
     // tiny problems: 8.5 against 36.5 us).  fp8 caches with M > 16 have no
     // warp-pair kernel and take the persistent per-warp partition.
     // PKD_FLAG_GRID, PKD_FLAG_FLAT and PKD_FLAG_BALANCED force a kernel.
@@ -128,8 +133,10 @@ pkd_status make_plan(int B, int sq, int Hq, int Hkv, int D, int P, int max_kv_le
         // chunks as the chunk limit allows, since each partial is M x D floats
         // (query_block_sq8: 4096-key chunks 193 us, 2048 216 us, 1024 246 us)
         const bool pair = pl.mma && pl.mt == 2 && !pl.flat && !pl.bal;
-        int splits = pair ? 1 : (kTargetCtas + units - 1) / units;
-        const int by_len = (pl.max_vis + kMaxChunk - 1) / kMaxChunk;
+        const bool fp8_grid = pl.mma && kv == PKD_FP8_E4M3 && !pl.flat;
+        const int max_chunk = fp8_grid ? pkd::kMaxCtaPages * P : kMaxChunk;
+        int splits = pair ? 1 : fp8_grid ? 2 * kFp8WaveCtas / units : (kTargetCtas + units - 1) / units;
+        const int by_len = (pl.max_vis + max_chunk - 1) / max_chunk;
         if (by_len > splits) splits = by_len;
         if (splits < 1) splits = 1;
         int chunk = (pl.max_vis + splits - 1) / splits;

@@ -65,6 +65,11 @@ def test_workspace_plan_is_a_host_function(lib):
     # ... while fp8 with M > 16 stays on the flat partition whatever the lengths
     assert pkd.workspace_size(64, 8, 32, 8, 128, 16, 4096, pkd.FP8_E4M3) == \
         pkd.workspace_size(64, 8, 32, 8, 128, 16, 131072, pkd.FP8_E4M3)
+    # the e4m3 grid fills at most two waves of 4 x 152 CTAs: 64 units of 131072 keys -> 19 chunks of 6912
+    assert pkd.workspace_size(8, 1, 64, 8, 128, 64, 131072, pkd.FP8_E4M3) == \
+        pkd.workspace_size(8, 1, 64, 8, 128, 64, 131072, pkd.FP8_E4M3, chunk_tokens=6912)
+    assert pkd.workspace_size(8, 1, 64, 8, 128, 64, 131072, pkd.FP8_E4M3) != \
+        pkd.workspace_size(8, 1, 64, 8, 128, 64, 131072, pkd.FP8_E4M3, chunk_tokens=6848)
     # batches above the flat kernel's table size use the chunked grid
     assert pkd.workspace_size(2048, 1, 32, 8, 128, 16, 4096, pkd.BF16) == \
         pkd.workspace_size(2048, 1, 32, 8, 128, 16, 4096, pkd.BF16, flags=pkd.FLAG_GRID)

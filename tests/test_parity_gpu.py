@@ -49,6 +49,7 @@ SMALL = {
     "bf16_d64_p32_auto": (dict(seq_lens=LENS, head_dim=64, page_size=32), dict()),
     "bf16_p48_not_power_of_two": (dict(seq_lens=LENS, page_size=48, window=300), dict()),
     "bf16_sq8_p48_not_power_of_two": (dict(seq_lens=LENS, sq=8, page_size=48), dict()),
+    "bf16_sq8_p48_chunk96": (dict(seq_lens=LENS, sq=8, page_size=48), dict(chunk_tokens=96)),
     "bf16_mha_g1": (dict(seq_lens=LENS, num_heads=8, num_kv_heads=8), dict(chunk_tokens=48)),
     "bf16_g2_sq1": (dict(seq_lens=LENS, num_heads=4, num_kv_heads=2), dict()),
     "bf16_g8": (dict(seq_lens=LENS, num_heads=64, num_kv_heads=8), dict(chunk_tokens=96)),
