@@ -37,6 +37,7 @@ def _check(case, tol=None, batch_index=None, **kw):
 
 
 LENS = [1, 15, 16, 17, 200, 1000, 777, 64, 0, 333]
+B50_LENS = [1000 + (i * 397) % 1049 for i in range(50)]
 
 SMALL = {
     # name: paged_case kwargs, call kwargs
@@ -50,6 +51,9 @@ SMALL = {
     "bf16_p48_not_power_of_two": (dict(seq_lens=LENS, page_size=48, window=300), dict()),
     "bf16_sq8_p48_not_power_of_two": (dict(seq_lens=LENS, sq=8, page_size=48), dict()),
     "bf16_sq8_p48_chunk96": (dict(seq_lens=LENS, sq=8, page_size=48), dict(chunk_tokens=96)),
+    # warp pairs over 50 requests of 1000-2048 keys
+    "bf16_sq8_b50": (dict(seq_lens=B50_LENS, sq=8), dict()),
+    "bf16_sq8_b50_window300_causal": (dict(seq_lens=B50_LENS, sq=8, window=300, causal=True), dict()),
     "bf16_mha_g1": (dict(seq_lens=LENS, num_heads=8, num_kv_heads=8), dict(chunk_tokens=48)),
     "bf16_g2_sq1": (dict(seq_lens=LENS, num_heads=4, num_kv_heads=2), dict()),
     "bf16_g8": (dict(seq_lens=LENS, num_heads=64, num_kv_heads=8), dict(chunk_tokens=96)),
