@@ -193,7 +193,7 @@ class PagedRunner:
         self.lse = torch.empty(case.q.shape[:3], dtype=torch.float32, device="cuda")
         self.max_kv_len = int(case.block_table.shape[1] * case.page_size)
         kv_code = {"bf16": pkd.BF16, "fp16": pkd.FP16, "fp8": pkd.FP8_E4M3}[case.dtype]
-        self.chunk, self.path, self.grid, self.flat = args.chunk, args.path, args.grid, args.flat
+        self.chunk, self.path, self.grid, self.flat = effective_chunk(case, args), args.path, args.grid, args.flat
         self.balanced = args.balanced
         flags = paged_flags(case, args, pkd)
         self.ws = torch.empty(pkd.workspace_size(case.batch, case.sq, case.num_heads, case.num_kv_heads,
@@ -520,8 +520,15 @@ def workload_config(case, args) -> dict:
                          "total": int(case.seq_lens.sum())},
             "pool_pages": case.num_pages, "l2": l2_note(args) + "; KV stream larger than L2",
             "parallelism": f"replicas{args.gpus}" if args.gpus > 1 else "single",
-            "kernel_path": getattr(args, "path", "auto"), "chunk_tokens": getattr(args, "chunk", 0),
+            "kernel_path": getattr(args, "path", "auto"), "chunk_tokens": effective_chunk(case, args),
             "kernel": paged_kernel_name(case, args)}
+
+
+def effective_chunk(case, args) -> int:
+    """Split-KV chunk of a run: --chunk if given, else the one the workload's
+    configuration fixes, else 0 (the library's plan)."""
+    chunk = getattr(args, "chunk", None)
+    return int(getattr(case, "chunk_tokens", 0)) if chunk is None else int(chunk)
 
 
 def paged_flags(case, args, pkd) -> int:
@@ -537,7 +544,7 @@ def paged_kernel_name(case, args) -> str:
         kv_code = {"bf16": pkd.BF16, "fp16": pkd.FP16, "fp8": pkd.FP8_E4M3}[case.dtype]
         return pkd.kernel_name(case.batch, case.sq, case.num_heads, case.num_kv_heads, case.head_dim,
                                case.page_size, int(case.block_table.shape[1] * case.page_size), kv_code,
-                               case.window, args.chunk, paged_flags(case, args, pkd))
+                               case.window, effective_chunk(case, args), paged_flags(case, args, pkd))
     except (OSError, RuntimeError) as e:  # library not built on this host
         return f"unknown ({e})"
 
@@ -556,7 +563,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="pkd", choices=["pkd", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--chunk", type=int, default=0, help="Split-KV chunk in keys (0 = the library's plan)")
+    ap.add_argument("--chunk", type=int, default=None,
+                    help="Split-KV chunk in keys (0 = the library's plan; default: the workload's own, else 0)")
     ap.add_argument("--path", default="auto", choices=["auto", "fma"],
                     help="library default (tensor cores for 16-bit caches) or CUDA cores")
     ap.add_argument("--grid", action="store_true", help="force the chunked grid (one CTA per Split-KV chunk)")

@@ -242,10 +242,13 @@ def test_query_block_sq8_sampled(window, variant):
     _check(case, batch_index=[0, 5, 11, 17, 23, 31], **VARIANTS[variant])
 
 
-@pytest.mark.parametrize("variant", ["auto", "grid", "flat_fma"])
+@pytest.mark.parametrize("variant", ["auto", "grid", "flat_fma", "configured_chunks"])
 def test_fp8_long_b8_sampled(variant):
     case = wl.fp8_long_b8()
-    _check(case, batch_index=[0, 7], **VARIANTS[variant])
+    if variant == "configured_chunks":  # 32 chunks of 4096 keys, as the workload fixes
+        _check(case, batch_index=[0, 7], chunk_tokens=case.chunk_tokens)
+    else:
+        _check(case, batch_index=[0, 7], **VARIANTS[variant])
 
 
 @pytest.mark.parametrize("sq", [1, 8])

@@ -95,6 +95,7 @@ class PagedCase:
     window: int = 0
     causal: bool = False
     poison_page: int = -1
+    chunk_tokens: int = 0    # Split-KV chunk the configuration fixes (0: the library's plan)
 
     @property
     def batch(self) -> int:
@@ -202,9 +203,11 @@ def query_block_sq8(window: int = 0) -> PagedCase:
 
 def fp8_long_b8(seq_len: int = 131072, batch: int = 8) -> PagedCase:
     seed = WORKLOAD_SEEDS["fp8_long_b8"]
-    return paged_case(name="fp8_long_b8", seq_lens=np.full(batch, seq_len, np.int32), sq=1,
+    case = paged_case(name="fp8_long_b8", seq_lens=np.full(batch, seq_len, np.int32), sq=1,
                       num_heads=64, num_kv_heads=8, head_dim=128, page_size=64, dtype="fp8",
                       seed=seed + 100)
+    case.chunk_tokens = 4096  # the configuration's Split-KV: 32 chunks of 4096 keys per sequence
+    return case
 
 
 @dataclasses.dataclass
