@@ -132,7 +132,9 @@ pkd_status pkd_workspace_check(void* workspace, size_t workspace_bytes, void* st
  * Split-KV [FA num_splits]: the keys of a (request, kv head) may be shared
  * between several workers whose partial results are merged by LSE inside
  * the same launch.  By default a chunked grid runs one CTA per chunk of
- * chunk_tokens keys (0: chosen by the library); for M = sq * num_heads /
+ * chunk_tokens keys (0: chosen by the library: about 2048 CTAs, chunks of at
+ * most 4096 keys; e4m3 caches at most two waves of 4 CTAs per SM, chunks up
+ * to 256 pages; M > 16 as few chunks of at most 4096 keys as possible); for M = sq * num_heads /
  * num_kv_heads > 16 two warps share each chunk's stages, 16 rows each.  fp8
  * caches with M > 16 run, for batch <= 1024, on a persistent grid that gives
  * every warp an equal slice of all requests' keys laid end to end.  PKD_FLAG_GRID, PKD_FLAG_FLAT and PKD_FLAG_BALANCED
