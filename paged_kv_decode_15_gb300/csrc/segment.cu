@@ -80,21 +80,48 @@ segmented_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     const long long row_base = static_cast<long long>(i) * (static_cast<long long>(p.topk) * p.bs + p.local);
     const int M = p.G;
 
-    if (tid < groups) {
-        const int cap = tid < p.topk ? p.bs : p.local;
-        int u = p.used[static_cast<long long>(i) * groups + tid];
-        u = u < 0 ? 0 : (u > cap ? cap : u);
-        sb[tid] = tid < p.topk ? p.bias[static_cast<long long>(i) * p.topk + tid] * kLog2e : 0.f;
-        if constexpr (kPaged) {
-            // keys [start, start + used) of request row i; stages start on 16-key boundaries
-            int st = p.seg_start[static_cast<long long>(i) * groups + tid];
-            st = st < 0 ? 0 : st;
-            if (st > p.max_kv_len) st = p.max_kv_len;
-            if (u > p.max_kv_len - st) u = p.max_kv_len - st;
-            ss[tid] = st;
-            sa[tid] = st / kStageTok * kStageTok;
+    if (warp == 0) {
+        // segments g = lane and lane + 32: used, prior, start; then their
+        // stage counts, scanned across the warp into the stage prefix
+        int cnt[2], incl[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int g = lane + 32 * h;
+            cnt[h] = 0;
+            if (g < groups) {
+                const int cap = g < p.topk ? p.bs : p.local;
+                int u = p.used[static_cast<long long>(i) * groups + g];
+                u = u < 0 ? 0 : (u > cap ? cap : u);
+                sb[g] = g < p.topk ? p.bias[static_cast<long long>(i) * p.topk + g] * kLog2e : 0.f;
+                if constexpr (kPaged) {
+                    // keys [start, start + used) of request row i; stages start on 16-key boundaries
+                    int st = p.seg_start[static_cast<long long>(i) * groups + g];
+                    st = st < 0 ? 0 : st;
+                    if (st > p.max_kv_len) st = p.max_kv_len;
+                    if (u > p.max_kv_len - st) u = p.max_kv_len - st;
+                    const int a = st / kStageTok * kStageTok;
+                    ss[g] = st;
+                    sa[g] = a;
+                    cnt[h] = u > 0 ? (st + u - a + kStageTok - 1) / kStageTok : 0;
+                } else {
+                    cnt[h] = (u + kStageTok - 1) / kStageTok;
+                }
+                su[g] = u;
+            }
+            incl[h] = cnt[h];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl[h], o);
+                if (lane >= o) incl[h] += v;
+            }
         }
-        su[tid] = u;
+        const int total0 = __shfl_sync(0xffffffffu, incl[0], 31);
+        incl[1] += total0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+            if (lane + 32 * h < groups) pre[lane + 32 * h] = incl[h] - cnt[h];
+        const int total = __shfl_sync(0xffffffffu, incl[1], 31);
+        if (lane == 0) pre[groups] = total < kMaxSegStages || !kPaged ? total : kMaxSegStages;
     }
     if (tid == 0) {
         for (int k = 0; k < kNW * kSegNbuf; ++k) mbar_init(smem_u32(bars + k), 1);
@@ -112,32 +139,7 @@ segmented_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             *reinterpret_cast<uint4*>(qs + r * S::QSTRIDE + v * 16) = val;
         }
     }
-    __syncthreads();
-    // stages of segment g (16 keys each; a paged segment may start mid-stage)
-    auto nstages = [&](int g) {
-        if (su[g] <= 0) return 0;
-        return kPaged ? (ss[g] + su[g] - sa[g] + kStageTok - 1) / kStageTok : (su[g] + kStageTok - 1) / kStageTok;
-    };
-    if (tid == 0) {
-        int acc = 0;
-        for (int g = 0; g < groups; ++g) {
-            pre[g] = acc;
-            acc += nstages(g);
-        }
-        pre[groups] = acc < kMaxSegStages || !kPaged ? acc : kMaxSegStages;
-    }
-    __syncthreads();
-    if constexpr (kPaged) {
-        // page of every stage, looked up once so that no TMA issue waits on the table
-        for (int s2 = tid; s2 < pre[groups]; s2 += blockDim.x) {
-            int g = 0;
-            while (g + 1 < groups && pre[g + 1] <= s2) ++g;
-            const int tok0 = sa[g] + (s2 - pre[g]) * kStageTok;
-            int pg = p.block_table[static_cast<long long>(i) * p.bt_stride + seg_page_col(p, tok0)];
-            spage[s2] = (pg < 0 || pg >= p.num_pages) ? -1 : pg;
-        }
-        __syncthreads();
-    }
+    __syncthreads();  // segments, stage prefix, q rows and barriers are in place
 
     // stage list of this warp: fused mode takes stages round-robin over the
     // union; segment-output mode takes whole segments g = warp, warp + 4, ...
@@ -231,6 +233,31 @@ segmented_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                 : "memory");
         }
     };
+    if constexpr (kPaged) {
+        // page of each of this warp's stages, looked up once so that no TMA
+        // issue waits on the table; a warp reads only its own stages' pages
+        for (int k = lane; k < my_n; k += 32) {
+            int g, sidx;
+            if constexpr (!kSegOut) {
+                const int s2 = warp + k * kNW;
+                g = 0;
+                while (g + 1 < groups && pre[g + 1] <= s2) ++g;
+                sidx = s2 - pre[g];
+            } else {
+                int before = 0;
+                g = warp;
+                while (g < groups && k - before >= pre[g + 1] - pre[g]) {
+                    before += pre[g + 1] - pre[g];
+                    g += kNW;
+                }
+                sidx = k - before;
+            }
+            const int tok0 = sa[g] + sidx * kStageTok;
+            const int pg = p.block_table[static_cast<long long>(i) * p.bt_stride + seg_page_col(p, tok0)];
+            spage[pre[g] + sidx] = (pg < 0 || pg >= p.num_pages) ? -1 : pg;
+        }
+        __syncwarp();
+    }
     if (lane == 0)
         for (int k = 0; k < kSegNbuf && k < my_n; ++k) issue(k);
 
