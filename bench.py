@@ -316,6 +316,80 @@ def segment_bytes(case) -> dict:
     return {"kv": kv, "total": kv + extra}
 
 
+def runner_kind(case):
+    import workloads as wl
+    return SegmentRunner if isinstance(case, wl.SegmentCase) else \
+        CacheWriteRunner if isinstance(case, wl.CacheWriteCase) else \
+        PagedSegmentRunner if isinstance(case, wl.PagedSegmentCase) else PagedRunner
+
+
+def make_flush(torch, args):
+    """Evict L2 before a step: write a buffer larger than L2; with write-read,
+    then read half of it back so that L2 holds clean lines and no write-back
+    of the flush is left to compete with the step."""
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    words = flush_buf.view(torch.int32)
+
+    class _Flush:
+        @staticmethod
+        def zero_():
+            flush_buf.zero_()
+            if args.l2_flush == "write-read":
+                words[:words.numel() // 2].amax()
+    return _Flush()
+
+
+# The other configurations, timed after the headline in the default run so
+# that one measured line carries them all (each with its own roofline figure).
+SECONDARY = ("query_block_sq8", "query_block_sq8_w4096", "fp8_long_b8", "dash_segments_n256", "dash_paged_n256",
+             "kv_write_32k")
+
+
+def run_secondary(args, peak_gbs) -> dict:
+    """Time each SECONDARY workload like the headline (L2 flushed before every
+    step, CUDA events on the launching stream, the workload's own Split-KV)."""
+    import copy
+    import torch
+    import paged_kv_decode_15_gb300 as pkd
+    import workloads as wl
+    flush = make_flush(torch, args)
+    stream = torch.cuda.current_stream()
+    sub_args = copy.copy(args)
+    sub_args.chunk, sub_args.path, sub_args.grid, sub_args.flat, sub_args.balanced = None, "auto", False, False, False
+    res = {}
+    for name in SECONDARY:
+        case = wl.WORKLOADS[name]()
+        runner = runner_kind(case)(case, sub_args, torch, pkd)
+        for _ in range(5):
+            flush.zero_()
+            runner.call()
+        torch.cuda.synchronize()
+        runner.check()
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.secondary_steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.secondary_steps)]
+        for i in range(args.secondary_steps):
+            flush.zero_()
+            starts[i].record(stream)
+            runner.call()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        runner.check()
+        ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+        avg = sum(ms) / len(ms) / 1e3
+        entry = {"us_per_call": round(avg * 1e6, 2), "us_per_call_median": round(statistics.median(ms) * 1e3, 2),
+                 "kv_gbs": round(runner.acct["kv"] / avg / 1e9, 1),
+                 "roofline_frac": round(runner.acct["total"] / avg / 1e9 / peak_gbs, 4),
+                 "algorithmic_bytes_per_launch": runner.acct["total"], "kernel": runner.kernel,
+                 "steps": args.secondary_steps}
+        if isinstance(runner, PagedRunner):
+            entry["paged_kernel"] = paged_kernel_name(case, sub_args)
+            entry["chunk_tokens"] = effective_chunk(case, sub_args)
+        res[name] = entry
+        del runner, case
+        torch.cuda.empty_cache()
+    return res
+
+
 def run_gpu(args, rank, world, dist):
     import torch
     import paged_kv_decode_15_gb300 as pkd
@@ -324,23 +398,8 @@ def run_gpu(args, rank, world, dist):
     pkd.build()
     pkd.load_library()
     case = wl.WORKLOADS[args.workload]()
-    kind = SegmentRunner if isinstance(case, wl.SegmentCase) else \
-        CacheWriteRunner if isinstance(case, wl.CacheWriteCase) else \
-        PagedSegmentRunner if isinstance(case, wl.PagedSegmentCase) else PagedRunner
-    runner = kind(case, args, torch, pkd)
-    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
-    words = flush_buf.view(torch.int32)
-
-    class _Flush:
-        """Evict L2 before a step: write a buffer larger than L2; with
-        write-read, then read half of it back so that L2 holds clean lines and
-        no write-back of the flush is left to compete with the step."""
-        @staticmethod
-        def zero_():
-            flush_buf.zero_()
-            if args.l2_flush == "write-read":
-                words[:words.numel() // 2].amax()
-    flush = _Flush()
+    runner = runner_kind(case)(case, args, torch, pkd)
+    flush = make_flush(torch, args)
     stream = torch.cuda.current_stream()
 
     for _ in range(args.warmup):
@@ -487,7 +546,7 @@ def run_reference(args, rank):
         total += _time_oracle(case, order[:n], threads)
     kv = algorithmic_bytes(sub)["kv"]
     value = kv * args.steps / total / 1e9
-    cfg = workload_config(case, args)
+    cfg = workload_config(case, args, gpu_kernel=False)
     sample = f"{n} of {case.batch} requests per step (all heads), fp64 C oracle, OpenMP over (request, head)"
     return {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 4), "higher_is_better": True,
@@ -498,7 +557,9 @@ def run_reference(args, rank):
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
-def workload_config(case, args) -> dict:
+def workload_config(case, args, gpu_kernel=True) -> dict:
+    """The workload's description; gpu_kernel=False (the oracle arm) leaves
+    out the library's kernel label, so that arm never loads the library."""
     if hasattr(case, "slots"):
         return {"workload": case.name, "num_tokens": case.num_tokens, "num_kv_heads": case.key.shape[1],
                 "head_dim": case.key.shape[2], "page_size": case.page_size, "in_dtype": case.in_dtype,
@@ -513,15 +574,19 @@ def workload_config(case, args) -> dict:
                 "head_dim": case.q.shape[2], "topk": case.topk, "bs": case.bs, "local": case.local,
                 "dtype": case.dtype, "used_rows": int(case.used.sum()),
                 "l2": l2_note(args)}
-    return {"workload": case.name, "batch": case.batch, "sq": case.sq, "num_heads": case.num_heads,
-            "num_kv_heads": case.num_kv_heads, "head_dim": case.head_dim, "page_size": case.page_size,
-            "kv_dtype": case.dtype, "window": case.window, "causal": case.causal,
-            "seq_lens": {"min": int(case.seq_lens.min()), "max": int(case.seq_lens.max()),
-                         "total": int(case.seq_lens.sum())},
-            "pool_pages": case.num_pages, "l2": l2_note(args) + "; KV stream larger than L2",
-            "parallelism": f"replicas{args.gpus}" if args.gpus > 1 else "single",
-            "kernel_path": getattr(args, "path", "auto"), "chunk_tokens": effective_chunk(case, args),
-            "kernel": paged_kernel_name(case, args)}
+    cfg = {"workload": case.name, "batch": case.batch, "sq": case.sq, "num_heads": case.num_heads,
+           "num_kv_heads": case.num_kv_heads, "head_dim": case.head_dim, "page_size": case.page_size,
+           "kv_dtype": case.dtype, "window": case.window, "causal": case.causal,
+           "scales": {"q": case.q_scale, "k": case.k_scale, "v": case.v_scale},
+           "seq_lens": {"min": int(case.seq_lens.min()), "max": int(case.seq_lens.max()),
+                        "total": int(case.seq_lens.sum())},
+           "pool_pages": case.num_pages, "l2": l2_note(args) + "; KV stream larger than L2",
+           "parallelism": f"replicas{args.gpus}" if args.gpus > 1 else "single",
+           "chunk_tokens": effective_chunk(case, args)}
+    if gpu_kernel:
+        cfg["kernel_path"] = getattr(args, "path", "auto")
+        cfg["kernel"] = paged_kernel_name(case, args)
+    return cfg
 
 
 def effective_chunk(case, args) -> int:
@@ -563,6 +628,9 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="pkd", choices=["pkd", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the other configurations' timings (run by default with the default workload on 1 GPU)")
+    ap.add_argument("--secondary-steps", type=int, default=100)
     ap.add_argument("--chunk", type=int, default=None,
                     help="Split-KV chunk in keys (0 = the library's plan; default: the workload's own, else 0)")
     ap.add_argument("--path", default="auto", choices=["auto", "fma"],
@@ -594,6 +662,7 @@ def main():
         dist = tdist
     case, runner, step_ms, total_ms, e2e_ms, h2d, d2h, clocks = run_gpu(args, rank, world, dist)
     acct = runner.acct
+    kind_is_paged = isinstance(runner, PagedRunner)
     if rank == 0:
         peaks = load_peaks()
         steps = args.steps
@@ -628,7 +697,10 @@ def main():
             "launch": getattr(args, "launch_mode", "direct"),
             "clocks": clocks,
         }
-        if not args.no_cpu_baseline and isinstance(runner, PagedRunner):
+        if not args.no_secondary and world == 1 and args.workload == DEFAULT_WORKLOAD:
+            del runner
+            line["secondary"] = run_secondary(args, peaks["hbm_gbs"])
+        if not args.no_cpu_baseline and kind_is_paged:
             line["cpu_baseline"] = cpu_baseline(case)
         print(json.dumps(line), flush=True)
     if dist:

@@ -7,6 +7,8 @@
  * Calls are asynchronous on the stream passed as `stream` (a cudaStream_t;
  * NULL is the legacy default stream).  All functions are thread-safe; the
  * message of the last failure is kept per host thread (pkd_last_error).
+ * A process may call the library on several GPUs: each kernel's launch
+ * set-up is made once per device, with that device current.
  *
  * Sources of the operations (vLLM API pages, by title and section):
  *   [TS]   vllm.v1.attention.backends.flashinfer_ts -- module docstring
@@ -50,6 +52,12 @@ typedef enum {
 #define PKD_FLAG_GRID 8u        /* the chunked grid: one CTA per Split-KV chunk */
 #define PKD_FLAG_FLAT 16u       /* the persistent flat partition whatever the shapes (batch <= 1024) */
 #define PKD_FLAG_BALANCED 32u   /* the persistent per-CTA partition (16-bit caches, tensor cores) */
+/* Diagnostic: every wait on a stage's copy tests its barrier once instead of
+ * waiting up to 200 ms, so a call reports PKD_ETIMEOUT whenever a copy has not
+ * landed by its first test.  The kernels still let every issued copy land
+ * before they leave.  It exists to exercise the timeout path; zero the
+ * workspace again (pkd_workspace_init) after such a call. */
+#define PKD_FLAG_TEST_TIMEOUT 64u
 
 /* Library version, major*10000 + minor*100 + patch. */
 int pkd_version(void);
@@ -133,8 +141,8 @@ pkd_status pkd_workspace_check(void* workspace, size_t workspace_bytes, void* st
  * between several workers whose partial results are merged by LSE inside
  * the same launch.  By default a chunked grid runs one CTA per chunk of
  * chunk_tokens keys (0: chosen by the library: about 2048 CTAs, chunks of at
- * most 4096 keys; e4m3 caches at most two waves of 4 CTAs per SM, chunks up
- * to 256 pages; M > 16 as few chunks of at most 4096 keys as possible); for M = sq * num_heads /
+ * most 4096 keys -- 32 chunks for 64 (request, kv head) units of 131,072
+ * keys; M > 16 as few chunks of at most 4096 keys as possible); for M = sq * num_heads /
  * num_kv_heads > 16 two warps share each chunk's stages, 16 rows each.  fp8
  * caches with M > 16 run, for batch <= 1024, on a persistent grid that gives
  * every warp an equal slice of all requests' keys laid end to end.  PKD_FLAG_GRID, PKD_FLAG_FLAT and PKD_FLAG_BALANCED
@@ -170,13 +178,19 @@ pkd_status pkd_paged_decode(const void* q, pkd_dtype q_dtype,
  * uses instead a scratch array compiled into the library: 32 MiB of device
  * memory that every GPU loading the library holds until the process exits.
  * A plan whose workspace (pkd_paged_decode_workspace_size) exceeds 32 MiB is
- * rejected with PKD_EUNSUPPORTED.  The call allocates nothing; it clears the
- * part of the scratch it uses (cudaMemsetAsync on `stream`) and launches the
- * decode kernel.  The first call on each device looks up the scratch
- * address on that device (make it before any stream capture).  All calls
- * share the one scratch array: calls that may overlap on the GPU (different
- * streams, or different host threads on one device) race and must be
- * serialised by the caller.  The device-side status word is not reported.
+ * rejected with PKD_EUNSUPPORTED.  fp8 caches with more than 16 query rows
+ * per kv head always are: their persistent per-warp kernel keeps two partial
+ * slots per worker warp whatever the batch (64 MiB at 32 rows).  The call
+ * allocates nothing; it clears the part of the scratch it uses
+ * (cudaMemsetAsync on `stream`) and launches the decode kernel.  The first
+ * call on each device looks up the scratch address on that device (make it
+ * before any stream capture); the address is kept for the process, so the
+ * call must not be used across a cudaDeviceReset.  All calls share the one
+ * scratch array: calls that may overlap on the GPU (different streams, or
+ * different host threads on one device) race and must be serialised by the
+ * caller.  The device-side status word (out-of-range lengths or pages, a
+ * wait that timed out) is cleared by the next call and never reported:
+ * callers that need it use pkd_paged_decode with their own workspace.
  */
 pkd_status pkd_paged_decode_static(const void* q, pkd_dtype q_dtype,
                                    const void* kv_cache, pkd_dtype kv_dtype, int64_t num_pages,

@@ -23,6 +23,7 @@ LIB_PATH = os.path.join(_HERE, "libpkd.so")
 OK, EINVAL, EUNSUPPORTED, ECUDA, EDEVICE_BOUNDS, ETIMEOUT = range(6)
 BF16, FP16, FP8_E4M3, FP32 = 0, 1, 2, 3
 FLAG_CAUSAL, FLAG_MMA_SMALL_M, FLAG_FMA, FLAG_GRID, FLAG_FLAT, FLAG_BALANCED = 1, 2, 4, 8, 16, 32
+FLAG_TEST_TIMEOUT = 64
 
 SYMBOLS = ("pkd_version", "pkd_last_error", "pkd_paged_decode_workspace_size", "pkd_paged_decode_kernel_name",
            "pkd_workspace_init",
@@ -162,13 +163,14 @@ def _workspace(nbytes: int, device) -> torch.Tensor:
 def paged_decode(q, kv_cache, block_table, seq_lens, scale, window=0, out=None, lse=None, *, q_scale=1.0,
                  k_scale=1.0, v_scale=1.0, max_kv_len=None, workspace=None, chunk_tokens=0, causal=False,
                  mma_small_m=False, force_fma=False, grid=False, flat=False, balanced=False, out_dtype=None,
-                 stream=None):
+                 test_timeout=False, stream=None):
     """Attention of each request's query block over its paged keys.
 
     q [B, sq, Hq, D]; kv_cache [num_pages, Hkv, P, 2*D] (bf16, fp16, or uint8 /
     float8_e4m3fn for fp8, with q of the same type); block_table int32 [B, W];
     seq_lens int32 [B].  Returns (out [B, sq, Hq, D], lse fp32 [B, sq, Hq]).
     max_kv_len defaults to the table's capacity W * P (no host sync).
+    test_timeout sets the diagnostic PKD_FLAG_TEST_TIMEOUT.
     """
     lib = load_library()
     for t, n in ((q, "q"), (kv_cache, "kv_cache"), (block_table, "block_table"), (seq_lens, "seq_lens")):
@@ -194,7 +196,7 @@ def paged_decode(q, kv_cache, block_table, seq_lens, scale, window=0, out=None, 
         max_kv_len = block_table.shape[1] * P
     flags = (FLAG_CAUSAL if causal else 0) | (FLAG_MMA_SMALL_M if mma_small_m else 0) | \
         (FLAG_FMA if force_fma else 0) | (FLAG_GRID if grid else 0) | (FLAG_FLAT if flat else 0) | \
-        (FLAG_BALANCED if balanced else 0)
+        (FLAG_BALANCED if balanced else 0) | (FLAG_TEST_TIMEOUT if test_timeout else 0)
     need = workspace_size(B, sq, Hq, Hkv, D, P, max_kv_len, kv_dt, window, chunk_tokens, flags)
     if workspace is None:
         workspace = _workspace(need, q.device)

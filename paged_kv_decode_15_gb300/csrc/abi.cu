@@ -13,6 +13,7 @@
 #include "../../include/pkd.h"
 #include "decode_common.cuh"
 #include "launch.h"
+#include "page_math.h"
 #include "segment.cuh"
 
 namespace {
@@ -44,11 +45,6 @@ int elt_bytes(pkd_dtype dt) { return dt == PKD_FP8_E4M3 ? 1 : dt == PKD_FP32 ? 4
 // gqa_decode_b64 (M = 4) 2048 (1024-key chunks) beats 512- to 2048-key chunks.
 constexpr int kTargetCtas = 2048;
 constexpr int kMaxChunk = 4096;    // and never puts more keys than this in one chunk
-// The e4m3 grid kernel holds four CTAs on each of GB300's 152 SMs; its chunks
-// fill at most two such waves (fp8_long_b8, 64 units of 131,072 keys: 19
-// chunks of 6912 keys, 1216 CTAs, 408 us against 429 us with 32 chunks of
-// 4096 and 423 us with 16 of 8192, whose second wave is two-thirds full).
-constexpr int kFp8WaveCtas = 4 * 152;
 constexpr size_t kHeader = 256;    // workspace status word lives in the first bytes
 
 struct Plan {
@@ -132,11 +128,12 @@ pkd_status make_plan(int B, int sq, int Hq, int Hkv, int D, int P, int max_kv_le
         // one-tile kernels: about kTargetCtas CTAs; warp pairs (M > 16): as few
         // chunks as the chunk limit allows, since each partial is M x D floats
         // (query_block_sq8: 4096-key chunks 193 us, 2048 216 us, 1024 246 us)
+        // (the e4m3 grid too: fp8_long_b8, 64 units of 131,072 keys, takes 32
+        // chunks of 4096, 364 us, against 373-392 us for chunks of 2048-3840
+        // and 378-400 us for 4416-8192)
         const bool pair = pl.mma && pl.mt == 2 && !pl.flat && !pl.bal;
-        const bool fp8_grid = pl.mma && kv == PKD_FP8_E4M3 && !pl.flat;
-        const int max_chunk = fp8_grid ? pkd::kMaxCtaPages * P : kMaxChunk;
-        int splits = pair ? 1 : fp8_grid ? 2 * kFp8WaveCtas / units : (kTargetCtas + units - 1) / units;
-        const int by_len = (pl.max_vis + max_chunk - 1) / max_chunk;
+        int splits = pair ? 1 : (kTargetCtas + units - 1) / units;
+        const int by_len = (pl.max_vis + kMaxChunk - 1) / kMaxChunk;
         if (by_len > splits) splits = by_len;
         if (splits < 1) splits = 1;
         int chunk = (pl.max_vis + splits - 1) / splits;
@@ -159,17 +156,7 @@ pkd_status make_plan(int B, int sq, int Hq, int Hkv, int D, int P, int max_kv_le
     return PKD_OK;
 }
 
-// Magic number for tok / P (0 <= tok < 2^31, 1 <= P < 2^31), division by an
-// invariant integer after Granlund and Montgomery: with l = ceil(log2 P),
-// m = floor(2^(31+l) / P) + 1 (2^31 when P is a power of two) and the shift
-// 31 + l, tok / P == (tok * m) >> (31 + l).
-void page_magic(int P, uint32_t& magic, int& shift) {
-    int l = 0;
-    while ((1LL << l) < P) ++l;
-    const bool pow2 = (P & (P - 1)) == 0;
-    magic = pow2 ? 0x80000000u : (uint32_t)(((uint64_t)1 << (31 + l)) / (uint64_t)P + 1);
-    shift = 31 + l;
-}
+using pkd::page_magic;
 
 // ---------------------------------------------------------- TMA descriptors
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -426,6 +413,7 @@ pkd_status pkd_paged_decode(const void* q, pkd_dtype q_dtype, const void* kv_cac
     page_magic(page_size, p.pmagic, p.pmshift);
     p.scale_log2 = scale * q_scale * k_scale * pkd::kLog2e;
     p.v_scale = v_scale;
+    p.wait_ns = (flags & PKD_FLAG_TEST_TIMEOUT) ? 0 : pkd::kWaitNs;
 
     cudaError_t e;
     cudaStream_t s = (cudaStream_t)stream;

@@ -8,22 +8,12 @@ template <class Body, int D>
 static cudaError_t launch_bal_one(const CUtensorMap& tmap, const DecodeParams& p, cudaStream_t stream) {
     using S = typename Body::S;
     auto kern = decode_bal_kernel<Body, D>;
-    static int per_sm = 0;  // benign race: every thread computes the same value
-    if (per_sm == 0) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
-        if (e != cudaSuccess) return e;
-        int n = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kNW * 32, S::SMEM);
-        if (e != cudaSuccess) return e;
-        per_sm = n > 0 ? n : 1;
-    }
-    int dev = 0, sms = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static PerDevice state;
+    int per_sm = 1, grid = 1;
+    cudaError_t e = kernel_setup(state, kern, kNW * 32, S::SMEM, &per_sm);
     if (e != cudaSuccess) return e;
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    e = persistent_grid(per_sm, kBalMaxCtas, grid);
     if (e != cudaSuccess) return e;
-    int grid = sms * per_sm;
-    if (grid > kBalMaxCtas) grid = kBalMaxCtas;
     kern<<<grid, kNW * 32, S::SMEM, stream>>>(tmap, p);
     return cudaGetLastError();
 }

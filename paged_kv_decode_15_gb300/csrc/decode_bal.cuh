@@ -86,10 +86,11 @@ struct WarpsBody {
         const int L = w.L;
         for (int k = 0; k < my_n; ++k) {
             const uint32_t u = u0 + k, buf = u % NBUF;
-            if (!mbar_wait(bar0 + 8 * buf, (u / NBUF) & 1, p.status)) {
+            if (!mbar_wait(bar0 + 8 * buf, (u / NBUF) & 1, p.status, p.wait_ns)) {
+                // let the issued copies (stages k .. k + NBUF - 1) land first
                 if (lane == 0) raise_status(p, kErrTimeout);
-                for (int j = k + 1; j < my_n && j < k + NBUF; ++j)
-                    mbar_wait(bar0 + 8 * ((u0 + j) % NBUF), ((u0 + j) / NBUF) & 1, p.status);
+                for (int j = k; j < my_n && j < k + NBUF; ++j)
+                    mbar_wait(bar0 + 8 * ((u0 + j) % NBUF), ((u0 + j) / NBUF) & 1);
                 return false;
             }
             const int tok0 = w.t0 + (warp + k * kNW) * kStageTok;
@@ -163,7 +164,7 @@ struct PairBody {
         int failed = 0;
         for (int k = 0; k < my_n; ++k) {
             const uint32_t u = u0 + k, buf = u % NBUF, parity = (u / NBUF) & 1;
-            if (!mbar_wait(full0 + 8 * buf, parity, p.status)) {
+            if (!mbar_wait(full0 + 8 * buf, parity, p.status, p.wait_ns)) {
                 failed = 1;
             } else {
                 const int tok0 = w.t0 + (pair + k * PAIRS) * kStageTok;
@@ -188,7 +189,7 @@ struct PairBody {
             if (__shfl_sync(kFull, failed, 0)) {
                 if (lane == 0) raise_status(p, kErrTimeout);
                 for (int j = k; j < my_n && j < k + NBUF; ++j)
-                    mbar_wait(full0 + 8 * ((u0 + j) % NBUF), ((u0 + j) / NBUF) & 1, p.status);
+                    mbar_wait(full0 + 8 * ((u0 + j) % NBUF), ((u0 + j) / NBUF) & 1);
                 return false;
             }
         }

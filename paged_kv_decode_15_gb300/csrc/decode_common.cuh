@@ -4,6 +4,7 @@
 // warps' partial softmax states and then, across CTAs, the Split-KV chunks.
 #pragma once
 
+#include "page_math.h"
 #include "ptx.cuh"
 
 namespace pkd {
@@ -35,6 +36,7 @@ struct DecodeParams {
     int pmshift;
     float scale_log2;            // scale * q_scale * k_scale * log2(e)
     float v_scale;
+    uint64_t wait_ns;            // limit of a wait on a stage's copy (0: test once)
 };
 
 struct CtaWork {
@@ -163,7 +165,7 @@ __device__ __forceinline__ bool row_sees(const DecodeParams& p, int L, int row, 
 // multiply by a magic number and a shift (division by an invariant integer,
 // Granlund and Montgomery, exact for every dividend below 2^31).
 __device__ __forceinline__ int page_col(const DecodeParams& p, int tok) {
-    return static_cast<int>((static_cast<unsigned long long>(static_cast<uint32_t>(tok)) * p.pmagic) >> p.pmshift);
+    return page_div(tok, p.pmagic, p.pmshift);
 }
 __device__ __forceinline__ int page_slot(const DecodeParams& p, int tok) { return tok - page_col(p, tok) * p.P; }
 

@@ -298,9 +298,10 @@ decode_flat_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams 
             wp.load_q(p, ub, uh, lane);
         }
         const int buf = k % NBUF;
-        if (__builtin_expect(!mbar_wait(bar0 + 8 * buf, (k / NBUF) & 1, p.status), 0)) {
+        if (__builtin_expect(!mbar_wait(bar0 + 8 * buf, (k / NBUF) & 1, p.status, p.wait_ns), 0)) {
+            // let the issued copies (stages k .. k + NBUF - 1) land first
             if (lane == 0) raise_status(p, kErrTimeout);
-            for (int j = k + 1; j < n && j < k + NBUF; ++j) mbar_wait(bar0 + 8 * (j % NBUF), (j / NBUF) & 1, p.status);
+            for (int j = k; j < n && j < k + NBUF; ++j) mbar_wait(bar0 + 8 * (j % NBUF), (j / NBUF) & 1);
             return;
         }
         const int tok0 = ulo + mk.s * kStageTok;

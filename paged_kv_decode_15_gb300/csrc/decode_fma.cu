@@ -10,12 +10,9 @@ template <int D, int KVT, int LPT, int MR>
 static cudaError_t launch_one(const CUtensorMap& tmap, const DecodeParams& p, dim3 grid, cudaStream_t stream) {
     using S = FmaShape<D, KVT, LPT, MR, kFmaNbuf>;
     auto kern = decode_fma_kernel<D, KVT, LPT, MR, kFmaNbuf>;
-    static bool configured = false;  // benign race: the attribute call is idempotent
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static PerDevice state;
+    cudaError_t e = kernel_setup(state, kern, kNW * 32, S::SMEM);
+    if (e != cudaSuccess) return e;
     kern<<<grid, kNW * 32, S::SMEM, stream>>>(tmap, p);
     return cudaGetLastError();
 }

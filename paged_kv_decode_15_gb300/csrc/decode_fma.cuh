@@ -75,7 +75,7 @@ decode_fma_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p
     int timed_out = 0, consumed = 0;
     for (int k = 0; k < my_n; ++k) {
         const int buf = k % NBUF;
-        if (!mbar_wait(bar0 + 8 * buf, (k / NBUF) & 1, p.status)) {
+        if (!mbar_wait(bar0 + 8 * buf, (k / NBUF) & 1, p.status, p.wait_ns)) {
             timed_out = 1;
             break;
         }
@@ -96,8 +96,8 @@ decode_fma_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p
     }
     if (timed_out) {
         if (lane == 0) raise_status(p, kErrTimeout);
-        for (int k = consumed + 1; k < my_n && k < consumed + NBUF; ++k)
-            mbar_wait(bar0 + 8 * (k % NBUF), (k / NBUF) & 1, p.status);
+        for (int k = consumed; k < my_n && k < consumed + NBUF; ++k)
+            mbar_wait(bar0 + 8 * (k % NBUF), (k / NBUF) & 1);
     }
 
     wp.finish();

@@ -13,12 +13,9 @@ template <class W, int D, int ELT, int NBUF>
 static cudaError_t launch_one(const CUtensorMap& tmap, const DecodeParams& p, dim3 grid, cudaStream_t stream) {
     using S = MmaShape<W, D, ELT, NBUF, kGridWarps>;
     auto kern = decode_mma_kernel<W, D, ELT, NBUF, kGridWarps>;
-    static bool configured = false;  // benign race: the attribute call is idempotent
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static PerDevice state;
+    cudaError_t e = kernel_setup(state, kern, kGridWarps * 32, S::SMEM);
+    if (e != cudaSuccess) return e;
     kern<<<grid, kGridWarps * 32, S::SMEM, stream>>>(tmap, p);
     return cudaGetLastError();
 }
@@ -27,12 +24,9 @@ template <int D, bool kBF16>
 static cudaError_t launch_pair(const CUtensorMap& tmap, const DecodeParams& p, dim3 grid, cudaStream_t stream) {
     using S = PairShape<D, kPairNbuf>;
     auto kern = decode_mma_pair_kernel<D, kBF16, kPairNbuf>;
-    static bool configured = false;  // benign race: the attribute call is idempotent
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static PerDevice state;
+    cudaError_t e = kernel_setup(state, kern, kNW * 32, S::SMEM);
+    if (e != cudaSuccess) return e;
     kern<<<grid, kNW * 32, S::SMEM, stream>>>(tmap, p);
     return cudaGetLastError();
 }

@@ -86,7 +86,7 @@ struct SpecPages {
 // Fp8MmaWarp (e4m3 caches; q fragments loaded by each warp, V widened in the
 // warp's scratch).
 template <class W, int D, int ELT, int NBUF, int NW = kNW>
-__global__ void __launch_bounds__(NW * 32)
+__global__ void __launch_bounds__(NW * 32, W::kMinBlocks)
 decode_mma_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p) {
     using S = MmaShape<W, D, ELT, NBUF, NW>;
     extern __shared__ uint8_t smem_raw[];
@@ -172,7 +172,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p
     int timed_out = 0, consumed = 0;
     for (int k = 0; k < my_n; ++k) {
         const int buf = k % NBUF;
-        if (!mbar_wait(bar0 + 8 * buf, (k / NBUF) & 1, p.status)) {
+        if (!mbar_wait(bar0 + 8 * buf, (k / NBUF) & 1, p.status, p.wait_ns)) {
             timed_out = 1;
             break;
         }
@@ -192,10 +192,12 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p
         }
     }
     if (timed_out) {
-        // let this warp's other copies land before the CTA leaves or reuses the ring
+        // let this warp's copies land before the CTA leaves or reuses the ring:
+        // stages consumed .. consumed + NBUF - 1 were issued (the first is the
+        // one whose wait gave up)
         if (lane == 0) raise_status(p, kErrTimeout);
-        for (int k = consumed + 1; k < my_n && k < consumed + NBUF; ++k)
-            mbar_wait(bar0 + 8 * (k % NBUF), (k / NBUF) & 1, p.status);
+        for (int k = consumed; k < my_n && k < consumed + NBUF; ++k)
+            mbar_wait(bar0 + 8 * (k % NBUF), (k / NBUF) & 1);
     }
 
     // ---- per-warp state to shared memory (the ring is reused for O)
@@ -311,7 +313,7 @@ decode_mma_pair_kernel(const __grid_constant__ CUtensorMap tmap, const DecodePar
     for (int k = 0; k < my_n; ++k) {
         const int buf = k % NBUF;
         const uint32_t parity = (k / NBUF) & 1;
-        if (!mbar_wait(full0 + 8 * buf, parity, p.status)) {
+        if (!mbar_wait(full0 + 8 * buf, parity, p.status, p.wait_ns)) {
             timed_out = 1;
             break;
         }
@@ -341,7 +343,7 @@ decode_mma_pair_kernel(const __grid_constant__ CUtensorMap tmap, const DecodePar
         // let this pair's other copies land before the CTA leaves or reuses the ring
         if (lane == 0) raise_status(p, kErrTimeout);
         for (int k = consumed; k < my_n && k < consumed + NBUF; ++k)
-            mbar_wait(full0 + 8 * (k % NBUF), (k / NBUF) & 1, p.status);
+            mbar_wait(full0 + 8 * (k % NBUF), (k / NBUF) & 1);
     }
 
     // ---- per-pair states to shared memory (the ring is reused for O)

@@ -1,11 +1,18 @@
 // Tensor-core warp for fp8-e4m3 caches.
 //
 // S = Q K^T runs directly on e4m3 operands (mma m16n8k32): q arrives already
-// quantised and the K tile is used as the TMA delivered it.  For O^T += V^T P^T
-// the V tile is widened once, in shared memory, to an fp16 tile of the same
-// swizzled layout (every e4m3 value is exact in fp16) and the fp16 warp runs
-// the softmax and P.V unchanged, so P is rounded only to fp16.  The q/k scales
-// stay in the logit scale and v_scale in the epilogue; all products are exact.
+// quantised and the K tile is used as the TMA delivered it.  O^T += V^T P^T
+// runs on fp16 operands (every e4m3 value is exact in fp16), with V widened
+// in registers, fragment by fragment, straight from the e4m3 stage:
+//   ldmatrix.trans of 16-bit units -- each unit a pair of e4m3 values of one
+//   key at dims (2j, 2j+1) -- gives lane (g, tg) the bytes
+//   V[2tg][2j], V[2tg][2j+1], V[2tg+1][2j], V[2tg+1][2j+1] with j = j0 + g;
+//   a byte permute pairs the two keys of one dim and cvt.f16x2.e4m3x2 widens
+//   them, which is an A fragment of V^T whose 16 rows are the dims
+//   2j0 .. 2j0+15 in the order (2j0, 2j0+2, ..., 2j0+14, 2j0+1, ..., 2j0+15).
+// The accumulator rows then hold dim pairs (MmaWarp's kPairRows layout), and
+// no V tile goes through shared memory twice.  P is rounded only to fp16;
+// the q/k scales stay in the logit scale and v_scale in the epilogue.
 #pragma once
 
 #include "mma_warp.cuh"
@@ -13,19 +20,15 @@
 namespace pkd {
 
 template <int MT, int NT>
-struct Fp8MmaWarp : MmaWarp<128, false, MT, NT> {
-    using Base = MmaWarp<128, false, MT, NT>;
-    static constexpr int kWide = 2 * 2048;  // one fp16 V tile: two 128-byte boxes of 16 rows
-    static constexpr int kScratchBytes = kWide;
-    static constexpr bool kCtaQ = false;  // e4m3 q fragments come straight from global memory
-    uint32_t q8[MT][4][4];                  // e4m3 A fragments, 4 k-steps of 32
-    uint32_t wide = 0;
-    uint8_t* wide_gen = nullptr;
+struct Fp8MmaWarp : MmaWarp<128, false, MT, NT, true> {
+    using Base = MmaWarp<128, false, MT, NT, true>;
+    static constexpr int kScratchBytes = 0;  // V is widened in registers
+    static constexpr bool kCtaQ = false;     // e4m3 q fragments come straight from global memory
+    // five CTAs per SM (96 registers): fp8_long_b8 at 32 chunks 363 us against 377 us with four
+    static constexpr int kMinBlocks = 5;
+    uint32_t q8[MT][4][4];                   // e4m3 A fragments, 4 k-steps of 32
 
-    __device__ __forceinline__ void setup(uint8_t* scratch) {
-        wide_gen = scratch;
-        wide = smem_u32(scratch);
-    }
+    __device__ __forceinline__ void setup(uint8_t*) {}
 
     // e4m3 q rows of (b, hk) as m16n8k32 A fragments (zero padding rows)
     __device__ __forceinline__ void load_q(const DecodeParams& p, int b, int hk, int lane) {
@@ -51,6 +54,29 @@ struct Fp8MmaWarp : MmaWarp<128, false, MT, NT> {
             }
     }
 
+    // O^T += V^T P^T with the e4m3 V tile at `vt` (16 keys x 128 bytes, 128-byte
+    // swizzle).  Load i covers the 16-byte chunks 2i and 2i+1 (dims 32i ..
+    // 32i+31) for keys 0-7 and 8-15: four 8x8 blocks of 16-bit units.
+    __device__ __forceinline__ void pv_e4m3(uint32_t vt, const uint32_t (&pb)[NT][2], int lane) {
+        const int mi = lane >> 3, ri = lane & 7;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint32_t r[4];
+            ldsm_x4_t(vt + swz((mi & 1) * 8 + ri, (2 * i + (mi >> 1)) * 16), r[0], r[1], r[2], r[3]);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                // r[2h]: keys 2tg, 2tg+1; r[2h+1]: keys 8+2tg, 8+2tg+1 (of chunk 2i+h)
+                uint32_t va[4];
+                va[0] = e4m3x2_to_f16x2(__byte_perm(r[2 * h], 0u, 0x0020));      // row g: dim 2j
+                va[1] = e4m3x2_to_f16x2(__byte_perm(r[2 * h], 0u, 0x0031));      // row g+8: dim 2j+1
+                va[2] = e4m3x2_to_f16x2(__byte_perm(r[2 * h + 1], 0u, 0x0020));
+                va[3] = e4m3x2_to_f16x2(__byte_perm(r[2 * h + 1], 0u, 0x0031));
+#pragma unroll
+                for (int n = 0; n < NT; ++n) mma16816<false>(this->oacc[2 * i + h][n], va, pb[n][0], pb[n][1]);
+            }
+        }
+    }
+
     template <class Visible>
     __device__ __forceinline__ void consume(uint32_t st, int half, int nvalid, bool masked, float scale2,
                                             float bias2, Visible visible, int lane) {
@@ -73,26 +99,12 @@ struct Fp8MmaWarp : MmaWarp<128, false, MT, NT> {
                 mma16832_e4m3(sacc[mt][1], q8[mt][kk], b10, b11);
             }
         }
-        // widen the V tile to fp16
-        const uint8_t* src = static_cast<const uint8_t*>(__cvta_shared_to_generic(st + half));
-#pragma unroll
-        for (int it = 0; it < 4; ++it) {
-            const int c = it * 32 + lane;  // 128 chunks of 16 e4m3: row, chunk
-            const int row = c >> 3, chunk = c & 7;
-            const uint4 v = *reinterpret_cast<const uint4*>(src + swz(row, chunk * 16));
-            const uint4 w0 = make_uint4(e4m3x2_to_f16x2(v.x & 0xffffu), e4m3x2_to_f16x2(v.x >> 16),
-                                        e4m3x2_to_f16x2(v.y & 0xffffu), e4m3x2_to_f16x2(v.y >> 16));
-            const uint4 w1 = make_uint4(e4m3x2_to_f16x2(v.z & 0xffffu), e4m3x2_to_f16x2(v.z >> 16),
-                                        e4m3x2_to_f16x2(v.w & 0xffffu), e4m3x2_to_f16x2(v.w >> 16));
-            *reinterpret_cast<uint4*>(wide_gen + swz(row, chunk * 32)) = w0;
-            *reinterpret_cast<uint4*>(wide_gen + swz(row, chunk * 32 + 16)) = w1;
-        }
-        __syncwarp();
+        uint32_t pb[NT][2];
         if (masked)
-            Base::template softmax_pv<true>(sacc, wide, nvalid, scale2, bias2, visible, lane);
+            Base::template softmax<true>(sacc, pb, nvalid, scale2, bias2, visible, lane);
         else
-            Base::template softmax_pv<false>(sacc, wide, nvalid, scale2, bias2, visible, lane);
-        __syncwarp();
+            Base::template softmax<false>(sacc, pb, nvalid, scale2, bias2, visible, lane);
+        pv_e4m3(st + half, pb, lane);
     }
 };
 

@@ -5,8 +5,47 @@
 #include <cuda_runtime.h>
 
 #include "../../include/pkd.h"
+#include "device_state.h"
 
 namespace pkd {
+
+// Set the dynamic shared-memory limit of `kern` on the current device, once
+// per device, and report how many CTAs of `threads` threads fit one SM there.
+template <class K>
+cudaError_t kernel_setup(PerDevice& state, K kern, int threads, int smem, int* per_sm = nullptr) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    cudaError_t err = cudaSuccess;
+    const int n = state.get(
+        dev,
+        [&]() -> int {
+            err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (err != cudaSuccess) return -1;
+            int b = 0;
+            err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kern, threads, smem);
+            if (err != cudaSuccess) return -1;
+            return b > 0 ? b : 1;  // a kernel that fits nowhere fails at launch
+        },
+        -2);
+    if (n == -2) return cudaErrorInvalidDevice;
+    if (n <= 0) return err;
+    if (per_sm) *per_sm = n;
+    return cudaSuccess;
+}
+
+// Resident CTAs of a persistent grid on the current device: SMs x per_sm.
+inline cudaError_t persistent_grid(int per_sm, int max_ctas, int& grid) {
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    grid = sms * per_sm;
+    if (grid > max_ctas) grid = max_ctas;
+    if (grid < 1) grid = 1;
+    return cudaSuccess;
+}
 
 struct DecodeParams;
 

@@ -13,7 +13,10 @@
 
 namespace pkd {
 
-template <int D, bool kBF16, int MT, int NT>
+// kPairRows: the P.V accumulator rows hold head-dim pairs (row r < 8 of a
+// 16-row tile is dim 2r, row 8 + r is dim 2r + 1), the layout the e4m3 warp's
+// register-widened V fragments give; otherwise row r is dim r.
+template <int D, bool kBF16, int MT, int NT, bool kPairRows = false>
 struct MmaWarp {
     // With two row tiles the Q fragments would not fit in registers next to
     // the accumulators: they are then staged in shared memory and re-read.
@@ -64,6 +67,7 @@ struct MmaWarp {
     static constexpr int kScratchBytes = kQSmem ? (MROWS * QSTRIDE + 1023) / 1024 * 1024 : 0;
     static constexpr int kNbuf = 2;  // ring depth per warp (three CTAs of four warps fit an SM)
     static constexpr bool kCtaQ = true;  // grid kernels stage q once for the CTA's warps
+    static constexpr int kMinBlocks = 1;  // CTAs per SM the grid kernel's register budget aims for
 
     __device__ __forceinline__ void setup(uint8_t* scratch) {
         qs_gen = scratch;
@@ -176,12 +180,27 @@ struct MmaWarp {
         }
     }
 
+    // Head dim of accumulator element c of d-tile dt held by lane group g.
+    static __device__ __forceinline__ int d_of(int dt, int g, int c) {
+        return kPairRows ? dt * 16 + 2 * g + (c >> 1) : dt * 16 + g + (c >> 1) * 8;
+    }
+
     // Online softmax of S (scaled here), then O^T += V^T P^T with the V tile at `vt`.
     template <bool kMasked, class Visible>
     __device__ __forceinline__ void softmax_pv(float (&sacc)[MT][2][4], uint32_t vt, int nvalid, float scale2,
                                                float bias2, Visible visible, int lane) {
+        uint32_t pb[NT][2];
+        softmax<kMasked>(sacc, pb, nvalid, scale2, bias2, visible, lane);
+        pv(vt, pb, lane);
+    }
+
+    // Online softmax of S: updates the row statistics, rescales O when a
+    // row's maximum moved, and returns P^T (rounded to the operand type) as
+    // the B fragments of the P.V product.
+    template <bool kMasked, class Visible>
+    __device__ __forceinline__ void softmax(float (&sacc)[MT][2][4], uint32_t (&pb)[NT][2], int nvalid,
+                                            float scale2, float bias2, Visible visible, int lane) {
         const int g = lane >> 2, tg = lane & 3;
-        const int mi = lane >> 3, ri = lane & 7;
         float alpha[MT][2];
         bool grew = false;
 #pragma unroll
@@ -242,13 +261,17 @@ struct MmaWarp {
                 }
             }
         }
-        uint32_t pb[NT][2];
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
             const int mt = n >> 1, h = n & 1;
             pb[n][0] = pack2<kBF16>(sacc[mt][0][2 * h], sacc[mt][0][2 * h + 1]);
             pb[n][1] = pack2<kBF16>(sacc[mt][1][2 * h], sacc[mt][1][2 * h + 1]);
         }
+    }
+
+    // O^T += V^T P^T for the 16-bit V tile at `vt` (A = V^T by ldmatrix.trans).
+    __device__ __forceinline__ void pv(uint32_t vt, const uint32_t (&pb)[NT][2], int lane) {
+        const int mi = lane >> 3, ri = lane & 7;
 #pragma unroll
         for (int dt = 0; dt < D / 16; ++dt) {
             uint32_t va[4];
@@ -294,7 +317,7 @@ struct MmaWarp {
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const float l = lcol[n][c & 1];
-                    f(n * 8 + 2 * tg + (c & 1), dt * 16 + g + (c >> 1) * 8, l > 0.f ? oacc[dt][n][c] / l : 0.f);
+                    f(n * 8 + 2 * tg + (c & 1), d_of(dt, g, c), l > 0.f ? oacc[dt][n][c] / l : 0.f);
                 }
     }
 
@@ -340,7 +363,7 @@ struct MmaWarp {
             for (int n = 0; n < NT; ++n)
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
-                    O[(n * 8 + 2 * tg + (c & 1)) * ostride + dt * 16 + g + (c >> 1) * 8] = oacc[dt][n][c];
+                    O[(n * 8 + 2 * tg + (c & 1)) * ostride + d_of(dt, g, c)] = oacc[dt][n][c];
     }
 };
 

@@ -56,6 +56,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test of phase `parity` (try_wait may suspend the thread for a
+// while; test_wait never does).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ uint64_t global_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
@@ -63,15 +77,20 @@ __device__ __forceinline__ uint64_t global_ns() {
 }
 
 // Wait for phase `parity` of a barrier.  Gives up (returns false) after
-// kWaitNs of wall time, or as soon as another CTA has reported a timeout in
+// limit_ns of wall time, or as soon as another CTA has reported a timeout in
 // the status word (when one is given), so a lost copy cannot hang the GPU.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const int32_t* status = nullptr) {
+// limit_ns == 0 tests the barrier once, without blocking.  Waits that must
+// let a warp's own copies land before it leaves (the drain after a timeout)
+// pass no status word.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const int32_t* status = nullptr,
+                                          uint64_t limit_ns = kWaitNs) {
+    if (limit_ns == 0) return mbar_test_wait(bar, parity);
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 255u) == 0u) {
-            if (global_ns() - t0 > kWaitNs) return false;
+            if (global_ns() - t0 > limit_ns) return false;
             if (status && (*reinterpret_cast<const volatile int32_t*>(status) & kErrTimeout)) return false;
         }
     }

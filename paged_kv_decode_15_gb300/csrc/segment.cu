@@ -41,7 +41,7 @@ struct SegShape {
 
 // tok / P by a magic-number multiply (exact for 0 <= tok < 2^31)
 __device__ __forceinline__ int seg_page_col(const SegmentParams& p, int tok) {
-    return static_cast<int>((static_cast<unsigned long long>(static_cast<uint32_t>(tok)) * p.pmagic) >> p.pmshift);
+    return page_div(tok, p.pmagic, p.pmshift);
 }
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -332,7 +332,7 @@ segmented_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     if (timed_out) {
         // this ABI has no status word: the warp stops, lets its other copies land
         // and leaves its share of the result incomplete
-        for (int k = consumed + 1; k < my_n && k < consumed + kSegNbuf; ++k)
+        for (int k = consumed; k < my_n && k < consumed + kSegNbuf; ++k)
             mbar_wait(bar0 + 8 * (k % kSegNbuf), (k / kSegNbuf) & 1);
     }
 
@@ -431,12 +431,9 @@ template <int D, bool kBF16, int NT, bool kSegOut, bool kPaged>
 static cudaError_t launch_seg_paged(const SegmentParams& p, cudaStream_t stream) {
     using S = SegShape<D, NT>;
     auto kern = segmented_kernel<D, kBF16, NT, kSegOut, kPaged>;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static PerDevice state;
+    cudaError_t e = kernel_setup(state, kern, kNW * 32, S::SMEM);
+    if (e != cudaSuccess) return e;
     kern<<<dim3(p.n, p.Hkv), kNW * 32, S::SMEM, stream>>>(p.kmap, p.vmap, p);
     return cudaGetLastError();
 }

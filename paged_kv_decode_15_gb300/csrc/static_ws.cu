@@ -10,6 +10,7 @@
 // itself allocates nothing.
 #include <cuda_runtime.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "../../include/pkd.h"
@@ -23,13 +24,15 @@ constexpr size_t kStaticScratchBytes = size_t(32) << 20;
 
 static __device__ __align__(256) unsigned char g_scratch[kStaticScratchBytes];
 
-constexpr int kMaxDevices = 64;
+using pkd::kMaxDevices;
 std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
 
 // Device address of g_scratch on the current device, looked up once per
 // device.  In host code the name g_scratch is only a host-side stand-in, so
-// the address must come from the runtime.
+// the address must come from the runtime.  The address is kept for the life
+// of the process: a device reset (cudaDeviceReset) reloads the module and may
+// move the array, so the static call must not be used across one.
 cudaError_t scratch_address(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -58,10 +61,14 @@ extern "C" pkd_status pkd_paged_decode_static(const void* q, pkd_dtype q_dtype, 
     const size_t need = pkd_paged_decode_workspace_size(batch, sq, num_heads, num_kv_heads, head_dim, page_size,
                                                         max_kv_len, kv_dtype, window, chunk_tokens, flags);
     if (need == 0) return PKD_EINVAL;  // the plan was rejected; pkd_last_error says why
-    if (need > kStaticScratchBytes)
-        return pkd::report(PKD_EUNSUPPORTED, "plan needs %zu bytes of scratch, above the static %zu; use "
-                           "pkd_paged_decode with a caller workspace, or a larger chunk_tokens", need,
-                           kStaticScratchBytes);
+    if (need > kStaticScratchBytes) {
+        const char* kern = pkd_paged_decode_kernel_name(batch, sq, num_heads, num_kv_heads, head_dim, page_size,
+                                                        max_kv_len, kv_dtype, window, chunk_tokens, flags);
+        const bool chunked = kern && std::strncmp(kern, "chunked grid", 12) == 0;
+        return pkd::report(PKD_EUNSUPPORTED, "the plan (%s) needs %zu bytes of scratch, above the static %zu; use "
+                           "pkd_paged_decode with a caller workspace%s", kern ? kern : "?", need,
+                           kStaticScratchBytes, chunked ? ", or a larger chunk_tokens" : "");
+    }
     void* scratch = nullptr;
     const cudaError_t e = scratch_address(&scratch);
     if (e != cudaSuccess)

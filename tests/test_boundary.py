@@ -4,6 +4,7 @@ any CUDA work (status codes and messages)."""
 import ctypes
 import os
 import re
+import subprocess
 
 import pytest
 
@@ -65,11 +66,11 @@ def test_workspace_plan_is_a_host_function(lib):
     # ... while fp8 with M > 16 stays on the flat partition whatever the lengths
     assert pkd.workspace_size(64, 8, 32, 8, 128, 16, 4096, pkd.FP8_E4M3) == \
         pkd.workspace_size(64, 8, 32, 8, 128, 16, 131072, pkd.FP8_E4M3)
-    # the e4m3 grid fills at most two waves of 4 x 152 CTAs: 64 units of 131072 keys -> 19 chunks of 6912
+    # the e4m3 grid takes the same rule: 64 units of 131072 keys -> 32 chunks of 4096
     assert pkd.workspace_size(8, 1, 64, 8, 128, 64, 131072, pkd.FP8_E4M3) == \
-        pkd.workspace_size(8, 1, 64, 8, 128, 64, 131072, pkd.FP8_E4M3, chunk_tokens=6912)
+        pkd.workspace_size(8, 1, 64, 8, 128, 64, 131072, pkd.FP8_E4M3, chunk_tokens=4096)
     assert pkd.workspace_size(8, 1, 64, 8, 128, 64, 131072, pkd.FP8_E4M3) != \
-        pkd.workspace_size(8, 1, 64, 8, 128, 64, 131072, pkd.FP8_E4M3, chunk_tokens=6848)
+        pkd.workspace_size(8, 1, 64, 8, 128, 64, 131072, pkd.FP8_E4M3, chunk_tokens=4032)
     # batches above the flat kernel's table size use the chunked grid
     assert pkd.workspace_size(2048, 1, 32, 8, 128, 16, 4096, pkd.BF16) == \
         pkd.workspace_size(2048, 1, 32, 8, 128, 16, 4096, pkd.BF16, flags=pkd.FLAG_GRID)
@@ -176,3 +177,28 @@ def test_kernel_name_follows_the_plan(lib):
     b2 = pkd.workspace_size(64, 1, 32, 8, 128, 16, 131072, pkd.BF16, flags=pkd.FLAG_BALANCED)
     assert b1 == b2 and b1 >= 512 * 2 * 4 * 128 * 4
     assert pkd.kernel_name(4096, 8, 32, 8, 128, 16, 4096, pkd.BF16, flags=pkd.FLAG_BALANCED).startswith("persistent")
+
+
+def test_launch_setup_is_kept_per_device(tmp_path):
+    """The per-device memo of kernel launch set-up, driven from eight host
+    threads on two stub devices (compiled with g++, no GPU)."""
+    src = os.path.join(ROOT, "tests", "device_state_check.cpp")
+    exe = str(tmp_path / "device_state_check")
+    csrc = os.path.join(ROOT, "paged_kv_decode_15_gb300", "csrc")
+    r = subprocess.run(["g++", "-std=c++17", "-O1", "-pthread", "-I", csrc, src, "-o", exe],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0 and r.stdout.startswith("ok"), r.stdout + r.stderr
+
+
+def test_page_division_by_magic_number_is_exact(tmp_path):
+    """tok / P and tok % P as the kernels compute them (multiply and shift)
+    against the integer division, for every page size up to 4096."""
+    src = os.path.join(ROOT, "tests", "page_math_check.cpp")
+    exe = str(tmp_path / "page_math_check")
+    csrc = os.path.join(ROOT, "paged_kv_decode_15_gb300", "csrc")
+    r = subprocess.run(["g++", "-std=c++17", "-O2", "-I", csrc, src, "-o", exe], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0 and r.stdout.startswith("ok"), r.stdout + r.stderr

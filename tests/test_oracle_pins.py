@@ -231,7 +231,7 @@ def test_windowed_equals_restricted_table_and_wide_window_is_none():
 
 
 def test_fp8_power_of_two_scales_equal_bf16_on_dequantised_values():
-    c = _small_case(dtype="fp8", seq_lens=[40, 64, 3])
+    c = _small_case(dtype="fp8", seq_lens=[40, 64, 3], fp8_scales="pow2")
     out, lse = _run(c)
     deq_cache = wl.round_to((brute.decode(c.kv_cache, "fp8") * c.k_scale).astype(np.float32), "bf16")
     deq_q = wl.round_to((brute.decode(c.q, "fp8") * c.q_scale).astype(np.float32), "bf16")
@@ -251,7 +251,10 @@ def test_fp8_power_of_two_scales_equal_bf16_on_dequantised_values():
     dict(sq=3, causal=True),
     dict(sq=3, causal=True, window=10),
     dict(dtype="fp16"),
-    dict(dtype="fp8"),
+    dict(dtype="fp8"),                       # q, K, V with three per-tensor scales amax/448
+    dict(dtype="fp8", fp8_scales="pow2"),
+    dict(scales=(0.731, 1.377, 0.589)),      # 16-bit storage with distinct q, k, v scales
+    dict(dtype="fp16", sq=3, scales=(1.7, 0.45, 2.3), causal=True),
     dict(head_dim=64, page_size=32, seq_lens=[70, 1, 33]),
 ])
 def test_paged_decode_matches_brute_force(kw):

@@ -1,7 +1,7 @@
 """GPU parity of paged decode against the fp64 oracle, through the C ABI.
 
 Small cases span several 16-key stages, several Split-KV chunks and ragged
-tails; full-size workloads are compared on all (or sampled) requests.  The
+tails; full-size workloads are compared on every request.  The
 probes check the page gather bit-exactly.
 """
 import zlib
@@ -71,7 +71,21 @@ SMALL = {
     "bf16_causal_sq8_m32_window": (dict(seq_lens=LENS, sq=8, causal=True, window=200), dict(chunk_tokens=64)),
     "bf16_causal_sq8_m32_auto": (dict(seq_lens=LENS, sq=8, causal=True), dict()),
     "fp16_sq6_g4_m24_p32": (dict(seq_lens=LENS, sq=6, dtype="fp16", page_size=32), dict(chunk_tokens=96)),
+    # q_scale, k_scale and v_scale all different and not powers of two: a
+    # kernel that swapped two of them, or dropped or squared one, fails here
+    # (bf16 keeps v_scale < 1 so that |out| stays where a bf16 ulp is < 1e-2)
+    "bf16_scales_qkv": (dict(seq_lens=LENS, scales=(0.731, 1.377, 0.589)), dict()),
+    "bf16_sq4_causal_scales_qkv": (dict(seq_lens=LENS, sq=4, causal=True, scales=(1.9, 0.53, 0.77)),
+                                   dict(chunk_tokens=64)),
+    "fp16_sq8_m32_scales_qkv": (dict(seq_lens=LENS, sq=8, dtype="fp16", scales=(1.7, 0.45, 2.3)), dict()),
+    "bf16_g8_window_scales_qkv": (dict(seq_lens=LENS, num_heads=64, window=100, scales=(0.61, 0.83, 0.97)),
+                                  dict(chunk_tokens=32)),
+    # fp8 caches: q, K and V with their own per-tensor scales amax/448 (the
+    # default of the generator), and the power-of-two shared scale
     "fp8_g8": (dict(seq_lens=LENS, dtype="fp8", num_heads=64, num_kv_heads=8), dict(chunk_tokens=64)),
+    "fp8_g8_pow2": (dict(seq_lens=LENS, dtype="fp8", num_heads=64, num_kv_heads=8, fp8_scales="pow2"),
+                    dict(chunk_tokens=64)),
+    "fp8_sq4_pow2": (dict(seq_lens=LENS, dtype="fp8", sq=4, fp8_scales="pow2"), dict()),
     "fp8_g4_p64": (dict(seq_lens=LENS, dtype="fp8", page_size=64), dict()),
     "fp8_g2_window": (dict(seq_lens=LENS, dtype="fp8", num_heads=16, num_kv_heads=8, window=100), dict()),
     "fp8_sq4_g4_m16": (dict(seq_lens=LENS, dtype="fp8", sq=4), dict()),
@@ -190,6 +204,46 @@ def test_bad_lengths_and_pages_raise_the_status_word():
     assert torch.isfinite(out.float()).all()
 
 
+@pytest.mark.parametrize("variant", ["auto", "pair", "flat", "balanced", "grid_fma"])
+def test_wait_timeout_is_reported_and_the_workspace_recovers(variant):
+    """With the diagnostic flag every wait on a stage's copy tests its barrier
+    once, so copies still in flight count as lost: the call must report
+    PKD_ETIMEOUT through the status word, leave a finite output, and (after
+    the workspace is zeroed again) a normal call must match the oracle.  No
+    copy is withheld: the kernels let every issued copy land before leaving."""
+    import paged_kv_decode_15_gb300 as pkd
+    sq = 8 if variant == "pair" else 1
+    vkw = {} if variant == "pair" else VARIANTS[variant]
+    lens = wl.uniform_lens(41, 48, 512, 4096)
+    case = wl.paged_case(name="timeout", seq_lens=lens, sq=sq, seed=42)
+    q = gu.to_dev(case.q, "bf16")
+    cache = gu.to_dev(case.kv_cache, "bf16")
+    bt = gu.to_dev(case.block_table, "int32")
+    dl = gu.to_dev(case.seq_lens, "int32")
+    flags = (pkd.FLAG_FLAT if vkw.get("flat") else 0) | (pkd.FLAG_BALANCED if vkw.get("balanced") else 0) | \
+        (pkd.FLAG_GRID if vkw.get("grid") else 0) | (pkd.FLAG_FMA if vkw.get("force_fma") else 0)
+    W = case.block_table.shape[1] * case.page_size
+    ws = torch.empty(pkd.workspace_size(case.batch, sq, 32, 8, 128, 16, W, pkd.BF16, flags=flags),
+                     dtype=torch.uint8, device="cuda")
+    pkd.workspace_init(ws)
+    out = torch.zeros(q.shape, dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros(q.shape[:3], dtype=torch.float32, device="cuda")
+    status = pkd.OK
+    for _ in range(3):  # a copy that lands before its first test is not a timeout: try again
+        pkd.paged_decode(q, cache, bt, dl, case.scale, 0, out=out, lse=lse, workspace=ws, test_timeout=True, **vkw)
+        status = pkd.workspace_check(ws)
+        if status == pkd.ETIMEOUT:
+            break
+    assert status == pkd.ETIMEOUT
+    assert torch.isfinite(out.float()).all()
+    pkd.workspace_init(ws)
+    out, lse = pkd.paged_decode(q, cache, bt, dl, case.scale, 0, workspace=ws, **vkw)
+    assert pkd.workspace_check(ws) == pkd.OK
+    ref, rlse = gu.oracle_paged(case)
+    gu.assert_close(out.double().cpu().numpy(), ref, gu.TOL_OUT, "after timeout out")
+    gu.assert_close(lse.double().cpu().numpy(), rlse, gu.TOL_LSE, "after timeout lse")
+
+
 def test_cuda_graph_replay_follows_new_lengths():
     """The call records no host state: a captured graph replays correctly when
     the lengths and the table change in place."""
@@ -235,20 +289,42 @@ def test_gqa_decode_b64_other_variants(variant):
     _check(case, **VARIANTS[variant])
 
 
+_FULL = {}
+
+
+def _full_case(name, make):
+    """A full-size workload and its oracle result, made once per module."""
+    if name not in _FULL:
+        case = make()
+        _FULL[name] = (case, gu.oracle_paged(case))
+    return _FULL[name]
+
+
+def _check_full(case, ref, **kw):
+    out, lse = gu.run_paged(case, **kw)
+    tol = gu.TOL_OUT_FP8 if case.dtype == "fp8" else gu.TOL_OUT
+    gu.assert_close(out, ref[0], tol, f"{case.name} out")
+    gu.assert_close(lse, ref[1], gu.TOL_LSE, f"{case.name} lse")
+
+
 @pytest.mark.parametrize("variant", ["auto", "grid", "balanced"])
 @pytest.mark.parametrize("window", [0, 4096])
-def test_query_block_sq8_sampled(window, variant):
-    case = wl.query_block_sq8(window=window)
-    _check(case, batch_index=[0, 5, 11, 17, 23, 31], **VARIANTS[variant])
+def test_query_block_sq8_full(window, variant):
+    """Every request of the query-block workload, both passes."""
+    case, ref = _full_case(f"qb{window}", lambda: wl.query_block_sq8(window=window))
+    _check_full(case, ref, **VARIANTS[variant])
 
 
 @pytest.mark.parametrize("variant", ["auto", "grid", "flat_fma", "configured_chunks"])
-def test_fp8_long_b8_sampled(variant):
-    case = wl.fp8_long_b8()
+def test_fp8_long_b8_full(variant):
+    """Every request of the long fp8 workload, whose q, K and V carry three
+    distinct per-tensor scales amax/448."""
+    case, ref = _full_case("fp8_long", wl.fp8_long_b8)
+    assert len({case.q_scale, case.k_scale, case.v_scale}) == 3
     if variant == "configured_chunks":  # 32 chunks of 4096 keys, as the workload fixes
-        _check(case, batch_index=[0, 7], chunk_tokens=case.chunk_tokens)
+        _check_full(case, ref, chunk_tokens=case.chunk_tokens)
     else:
-        _check(case, batch_index=[0, 7], **VARIANTS[variant])
+        _check_full(case, ref, **VARIANTS[variant])
 
 
 @pytest.mark.parametrize("sq", [1, 8])
@@ -262,7 +338,25 @@ def test_long_slices_reload_the_page_list(sq):
 
 @pytest.mark.parametrize("dtype,sq", [("fp8", 1), ("bf16", 8)])
 def test_batch_above_the_flat_table_limit(dtype, sq):
-    """1500 short requests: the chunked grid (e4m3 warp, or warp pairs for 32 rows)."""
+    """1500 short requests (0-69 keys): the chunked grid (e4m3 warp, or warp
+    pairs for 32 rows).  With so few keys many outputs lie near |4|, where half
+    a bf16 ulp alone is 0.0078, so the arithmetic is compared on the fp32
+    output (at the bf16 tolerance) and the 16-bit output is checked to be that
+    fp32 output rounded to nearest even, bit for bit."""
+    import paged_kv_decode_15_gb300 as pkd
     lens = np.random.default_rng(77).integers(0, 70, size=1500).astype(np.int32)
     case = wl.paged_case(name="wide", seq_lens=lens, sq=sq, dtype=dtype, seed=78)
-    _check(case, batch_index=list(range(0, 1500, 97)))
+    ref, rlse = gu.oracle_paged(case)
+    q = gu.to_dev(case.q, dtype)
+    cache = gu.to_dev(case.kv_cache, dtype)
+    bt = gu.to_dev(case.block_table, "int32")
+    dl = gu.to_dev(case.seq_lens, "int32")
+    kw = dict(q_scale=case.q_scale, k_scale=case.k_scale, v_scale=case.v_scale)
+    o32, lse = pkd.paged_decode(q, cache, bt, dl, case.scale, 0, out_dtype=torch.float32, **kw)
+    o16, lse16 = pkd.paged_decode(q, cache, bt, dl, case.scale, 0, out_dtype=torch.bfloat16, **kw)
+    torch.cuda.synchronize()
+    tol = gu.TOL_OUT_FP8 if dtype == "fp8" else gu.TOL_OUT
+    gu.assert_close(o32.double().cpu().numpy(), ref, tol, "wide out (fp32)")
+    gu.assert_close(lse.double().cpu().numpy(), rlse, gu.TOL_LSE, "wide lse")
+    assert torch.equal(o16.cpu().view(torch.int16), o32.cpu().to(torch.bfloat16).view(torch.int16))
+    assert torch.equal(lse16.cpu(), lse.cpu())

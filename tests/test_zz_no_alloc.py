@@ -25,39 +25,55 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else None
 
 
-def _args(case, d, out, lse):
-    import paged_kv_decode_15_gb300 as pkd
-    return [_ptr(d["q"]), pkd.BF16, _ptr(d["cache"]), pkd.BF16, case.num_pages, _ptr(d["bt"]),
+def _args(case, d, out, lse, dt):
+    return [_ptr(d["q"]), dt, _ptr(d["cache"]), dt, case.num_pages, _ptr(d["bt"]),
             d["bt"].stride(0), _ptr(d["lens"]), case.batch, case.sq, case.num_heads, case.num_kv_heads,
-            case.head_dim, case.page_size, d["max_kv_len"], case.scale, 1.0, 1.0, 1.0, case.window,
-            _ptr(out), pkd.BF16, _ptr(lse)]
+            case.head_dim, case.page_size, d["max_kv_len"], case.scale, case.q_scale, case.k_scale, case.v_scale,
+            case.window, _ptr(out), 0, _ptr(lse)]
 
 
-def test_static_scratch_matches_caller_workspace_twice():
+# (cache type, Split-KV chunk, flags name): the bf16 chunked grid with a fixed
+# chunk, the persistent per-CTA partition, and the e4m3 grid with its own plan
+PLANS = [("bf16", 256, None), ("bf16", 0, "FLAG_BALANCED"), ("fp8", 0, None)]
+
+
+@pytest.mark.parametrize("dtype,chunk,flag", PLANS)
+def test_static_scratch_matches_caller_workspace_twice(dtype, chunk, flag):
     import paged_kv_decode_15_gb300 as pkd
     pkd.build()
     lib = pkd.load_library()
-    case = wl.paged_case(name="static", seq_lens=[4000, 700, 2600, 33, 4096, 1500], seed=77, table_width=256)
-    d = dict(q=gu.to_dev(case.q, "bf16"), cache=gu.to_dev(case.kv_cache, "bf16"),
+    flags = getattr(pkd, flag) if flag else 0
+    dt = {"bf16": pkd.BF16, "fp8": pkd.FP8_E4M3}[dtype]
+    case = wl.paged_case(name="static", seq_lens=[4000, 700, 2600, 33, 4096, 1500], seed=77, table_width=256,
+                         dtype=dtype)
+    d = dict(q=gu.to_dev(case.q, dtype), cache=gu.to_dev(case.kv_cache, dtype),
              bt=gu.to_dev(case.block_table, "int32"), lens=gu.to_dev(case.seq_lens, "int32"), max_kv_len=4096)
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     shape = case.q.shape
-    ws = torch.empty(pkd.workspace_size(case.batch, 1, 32, 8, 128, 16, 4096, pkd.BF16), dtype=torch.uint8,
-                     device="cuda")
+    ws = torch.empty(pkd.workspace_size(case.batch, 1, 32, 8, 128, 16, 4096, dt, chunk_tokens=chunk, flags=flags),
+                     dtype=torch.uint8, device="cuda")
     pkd.workspace_init(ws)
+    free = []
     for lens in ([4000, 700, 2600, 33, 4096, 1500], [64, 4096, 17, 3000, 0, 2222]):
         d["lens"].copy_(torch.tensor(lens, dtype=torch.int32))
         ref = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
         ref_lse = torch.empty(shape[:3], dtype=torch.float32, device="cuda")
         got = torch.empty_like(ref)
         got_lse = torch.empty_like(ref_lse)
-        st = lib.pkd_paged_decode(*_args(case, d, ref, ref_lse), _ptr(ws), ws.numel(), 256, 0, stream)
-        assert st == pkd.OK, lib.pkd_last_error()
-        st = lib.pkd_paged_decode_static(*_args(case, d, got, got_lse), 256, 0, stream)
+        st = lib.pkd_paged_decode(*_args(case, d, ref, ref_lse, dt), _ptr(ws), ws.numel(), chunk, flags, stream)
         assert st == pkd.OK, lib.pkd_last_error()
         torch.cuda.synchronize()
-        gu.assert_close(got.double().cpu().numpy(), ref.double().cpu().numpy(), gu.TOL_OUT, "static out")
+        before = torch.cuda.mem_get_info()[0]
+        st = lib.pkd_paged_decode_static(*_args(case, d, got, got_lse, dt), chunk, flags, stream)
+        assert st == pkd.OK, lib.pkd_last_error()
+        torch.cuda.synchronize()
+        free.append(torch.cuda.mem_get_info()[0] - before)
+        tol = gu.TOL_OUT_FP8 if dtype == "fp8" else gu.TOL_OUT
+        gu.assert_close(got.double().cpu().numpy(), ref.double().cpu().numpy(), tol, "static out")
         gu.assert_close(got_lse.double().cpu().numpy(), ref_lse.double().cpu().numpy(), gu.TOL_LSE, "static lse")
+    # the first static call on a device may load the library's module (and
+    # with it the scratch array); the second call allocates nothing at all
+    assert free[1] == 0, f"device memory changed by {free[1]} bytes across a static call"
 
 
 def test_static_scratch_rejects_plans_above_its_size():

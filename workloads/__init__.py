@@ -16,11 +16,13 @@ Workloads (named by what they are):
                          (``window=4096`` gives the windowed second pass)
   dash_segments_n256     n=256, Hq=32, Hkv=8, D=128, topk=8, bs=64, local=128
   fp8_long_b8            B=8, sq=1, Hq=64, Hkv=8, D=128, P=64, L=131072, fp8-e4m3
+                         with per-tensor scales amax/448 for q, K and V
 """
 from __future__ import annotations
 
 import dataclasses
 import math
+import os
 
 import numpy as np
 import torch
@@ -28,9 +30,11 @@ import torch
 BF16_NAN = 0x7FC0
 FP16_NAN = 0x7E00
 FP8_NAN = 0x7F
-# fp8 per-tensor scale: a power of two just above amax/448 for N(0,1) samples
-# of this size (amax ~ 6.1), so dequantisation is exact in any precision.
+# fp8 power-of-two scale: just above amax/448 for N(0,1) samples of this size
+# (amax ~ 6.1), so dequantisation is exact in any precision.  The fp8
+# workloads use per-tensor scales amax/448 instead (paged_case, fp8_scales="amax").
 FP8_SCALE = 1.0 / 64.0
+E4M3_MAX = 448.0
 
 SEED_BASE = 1000
 WORKLOAD_SEEDS = {
@@ -72,6 +76,63 @@ def normal_storage(rng: np.random.Generator, shape, dtype: str, scale: float = 1
         e = min(n, s + chunk)
         out[s:e] = round_to(rng.standard_normal(e - s, dtype=np.float32), dtype, scale)
     return out.reshape(shape)
+
+
+def amax_scale(amax) -> float:
+    """Per-tensor fp8 scale amax / 448, as an fp32 value."""
+    return float(np.float32(amax) / np.float32(E4M3_MAX))
+
+
+def _parallel(fn, items, threads=None):
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(max_workers=threads or min(32, os.cpu_count() or 1)) as ex:
+        return list(ex.map(fn, items))
+
+
+def fp8_kv_pool(seed: int, shape, chunk_rows: int = 1 << 16):
+    """A pool [..., 2*D] of N(0,1) key/value rows quantised to e4m3 with
+    per-tensor scales: k_scale = amax(K)/448 over every key half of the pool,
+    v_scale = amax(V)/448 over every value half.
+
+    Each block of chunk_rows rows is drawn from its own seeded stream, once to
+    find the two maxima and again to quantise, so the pool is never held in
+    fp32.  Returns (uint8 storage, k_scale, v_scale).
+    """
+    twoD = int(shape[-1])
+    D = twoD // 2
+    rows = int(np.prod(shape[:-1]))
+    starts = list(range(0, rows, chunk_rows))
+    seeds = np.random.SeedSequence([int(seed), 0xF8]).spawn(len(starts))
+
+    def draw(i):
+        n = min(chunk_rows, rows - starts[i])
+        return np.random.default_rng(seeds[i]).standard_normal((n, twoD), dtype=np.float32)
+
+    def maxima(i):
+        x = np.abs(draw(i))
+        return float(x[:, :D].max()), float(x[:, D:].max())
+
+    m = _parallel(maxima, range(len(starts)))
+    k_scale = amax_scale(max(a for a, _ in m))
+    v_scale = amax_scale(max(b for _, b in m))
+    out = np.empty((rows, twoD), np.uint8)
+
+    def fill(i):
+        x = draw(i)
+        s = starts[i]
+        out[s:s + x.shape[0], :D] = round_to(x[:, :D], "fp8", k_scale)
+        out[s:s + x.shape[0], D:] = round_to(x[:, D:], "fp8", v_scale)
+
+    _parallel(fill, range(len(starts)))
+    return out.reshape(shape), k_scale, v_scale
+
+
+def fp8_quantised(rng: np.random.Generator, shape):
+    """N(0,1) samples quantised to e4m3 with the per-tensor scale amax/448.
+    Returns (uint8 storage, scale)."""
+    x = rng.standard_normal(int(np.prod(shape)), dtype=np.float32)
+    scale = amax_scale(np.abs(x).max()) if x.size else 1.0
+    return round_to(x, "fp8", scale).reshape(shape), scale
 
 
 @dataclasses.dataclass
@@ -119,7 +180,7 @@ class PagedCase:
 def paged_case(*, name="paged", seq_lens, sq=1, num_heads=32, num_kv_heads=8, head_dim=128,
                page_size=16, dtype="bf16", seed=0, pool_factor=1.25, window=0, causal=False,
                poison_tail=True, table_width=None, scale=None, fp8_scale=FP8_SCALE,
-               spare_pages=1) -> PagedCase:
+               spare_pages=1, fp8_scales="amax", scales=None) -> PagedCase:
     """Build a paged-decode problem.
 
     The pool holds ceil(pool_factor * sum ceil(L/P)) data pages plus one
@@ -128,6 +189,12 @@ def paged_case(*, name="paged", seq_lens, sq=1, num_heads=32, num_kv_heads=8, he
     columns past a request's last page point at the NaN page, and (with
     ``poison_tail``) the slots past L in a request's last page are NaN too, so
     any read outside the visible keys shows up in the output.
+
+    fp8 caches: with fp8_scales="amax" (default) K, V and the pre-quantised q
+    each get their own per-tensor scale amax/448 (three distinct scales that
+    are not powers of two); with "pow2" all three share the power of two
+    ``fp8_scale``.  ``scales=(q_scale, k_scale, v_scale)`` sets the three
+    scalars of a 16-bit case (1.0 each by default).
     """
     rng = np.random.default_rng(seed)
     lens = np.asarray(seq_lens, dtype=np.int32).reshape(-1)
@@ -138,9 +205,20 @@ def paged_case(*, name="paged", seq_lens, sq=1, num_heads=32, num_kv_heads=8, he
     num_pages = n_data + 1
     poison = n_data  # the last page of the pool is all NaN
     W = table_width or max(1, max(pages_needed) if B else 1)
+    per_tensor = dtype == "fp8" and fp8_scales == "amax"
+    if dtype == "fp8" and fp8_scales not in ("amax", "pow2"):
+        raise ValueError(fp8_scales)
     scale_kv = fp8_scale if dtype == "fp8" else 1.0
+    q_scale = k_scale = v_scale = scale_kv
+    if scales is not None:
+        if dtype == "fp8":
+            raise ValueError("fp8 scales come from the data (fp8_scales)")
+        q_scale, k_scale, v_scale = (float(x) for x in scales)
 
-    cache = normal_storage(rng, (num_pages, Hkv, P, 2 * D), dtype, scale_kv)
+    if per_tensor:
+        cache, k_scale, v_scale = fp8_kv_pool(seed, (num_pages, Hkv, P, 2 * D))
+    else:
+        cache = normal_storage(rng, (num_pages, Hkv, P, 2 * D), dtype, scale_kv)
     cache[poison] = _nan_bits(dtype)
     perm = rng.permutation(n_data).astype(np.int32)
     table = np.full((B, W), poison, dtype=np.int32)
@@ -151,12 +229,15 @@ def paged_case(*, name="paged", seq_lens, sq=1, num_heads=32, num_kv_heads=8, he
         cursor += k
         if poison_tail and k > 0 and lens[b] % P:
             cache[table[b, k - 1], :, lens[b] % P:, :] = _nan_bits(dtype)
-    q = normal_storage(rng, (B, sq, num_heads, D), dtype, scale_kv)
+    if per_tensor:
+        q, q_scale = fp8_quantised(rng, (B, sq, num_heads, D))
+    else:
+        q = normal_storage(rng, (B, sq, num_heads, D), dtype, scale_kv)
     return PagedCase(
         name=name, q=q, kv_cache=cache, block_table=table, seq_lens=lens, dtype=dtype, sq=int(sq),
         num_heads=int(num_heads), num_kv_heads=Hkv, head_dim=D, page_size=P,
         scale=float(scale if scale is not None else D ** -0.5),
-        q_scale=scale_kv, k_scale=scale_kv, v_scale=scale_kv,
+        q_scale=q_scale, k_scale=k_scale, v_scale=v_scale,
         window=int(window), causal=bool(causal), poison_page=poison)
 
 
