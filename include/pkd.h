@@ -142,8 +142,15 @@ pkd_status pkd_workspace_check(void* workspace, size_t workspace_bytes, void* st
  * the same launch.  By default a chunked grid runs one CTA per chunk of
  * chunk_tokens keys (0: chosen by the library: about 2048 CTAs, chunks of at
  * most 4096 keys -- 32 chunks for 64 (request, kv head) units of 131,072
- * keys; M > 16 as few chunks of at most 4096 keys as possible); for M = sq * num_heads /
- * num_kv_heads > 16 two warps share each chunk's stages, 16 rows each.  fp8
+ * keys).  16-bit query blocks of M = sq * num_heads / num_kv_heads = 17-32
+ * rows with head_dim 128, no causal mask and batch <= 512 run instead on a
+ * persistent kernel with one CTA per SM on the tcgen05 tensor cores: work
+ * items of at most chunk_tokens keys (0: 1024; at most 2048), equal within a
+ * request, taken from a queue in the workspace; the chunk partials of split
+ * requests are merged by a second, short kernel on the same stream (so such
+ * calls launch two kernels).  Other 16-bit blocks of 17-32 rows run the
+ * chunked grid with two warps sharing each chunk's stages, 16 rows each
+ * (as few chunks of at most 4096 keys as possible).  fp8
  * caches with M > 16 run, for batch <= 1024, on a persistent grid that gives
  * every warp an equal slice of all requests' keys laid end to end.  PKD_FLAG_GRID, PKD_FLAG_FLAT and PKD_FLAG_BALANCED
  * (a persistent grid with an equal slice per CTA) force a kernel;

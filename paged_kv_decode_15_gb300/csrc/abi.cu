@@ -12,6 +12,7 @@
 
 #include "../../include/pkd.h"
 #include "decode_common.cuh"
+#include "decode_tc05.cuh"
 #include "launch.h"
 #include "page_math.h"
 #include "segment.cuh"
@@ -45,12 +46,16 @@ int elt_bytes(pkd_dtype dt) { return dt == PKD_FP8_E4M3 ? 1 : dt == PKD_FP32 ? 4
 // gqa_decode_b64 (M = 4) 2048 (1024-key chunks) beats 512- to 2048-key chunks.
 constexpr int kTargetCtas = 2048;
 constexpr int kMaxChunk = 4096;    // and never puts more keys than this in one chunk
-constexpr size_t kHeader = 256;    // workspace status word lives in the first bytes
+constexpr size_t kHeader = 256;    // workspace status word lives in the first bytes (and the
+                                   // tcgen05 kernel's work queue at byte 64)
+// Work items of the tcgen05 kernel: chunks of at most this many keys.
+constexpr int kTcChunk = 1024;
 
 struct Plan {
     bool mma;
     bool flat;     // persistent per-warp partition
     bool bal;      // persistent per-CTA partition
+    bool tc;       // persistent tcgen05 kernel (query blocks of 17-32 rows)
     int M, G;
     int mt, nt;    // tensor-core tiles
     int lpt, mr;   // CUDA-core lanes per key, padded rows
@@ -91,6 +96,11 @@ pkd_status make_plan(int B, int sq, int Hq, int Hkv, int D, int P, int max_kv_le
     }
     pl.flat = !pl.bal && B <= pkd::kFlatMaxBatch && !(flags & PKD_FLAG_GRID) &&
               ((flags & PKD_FLAG_FLAT) || flat_default);
+    // 16-bit query blocks of 17-32 rows without a causal mask: the tcgen05
+    // kernel (query_block_sq8: see the kernel-choice table of the design notes)
+    pl.tc = !pl.bal && !pl.flat && (kv == PKD_BF16 || kv == PKD_FP16) && D == 128 && sq * (Hq / Hkv) > 16 &&
+            sq * (Hq / Hkv) <= 32 && B <= pkd::kTcMaxBatch && !(flags & (PKD_FLAG_GRID | PKD_FLAG_FMA | PKD_FLAG_CAUSAL)) &&
+            (chunk_tokens <= 0 || chunk_tokens <= pkd::kTcMaxChunk);
     if (kv == PKD_FP8_E4M3 && (flags & PKD_FLAG_FMA)) {
         if (M > 8) return fail(PKD_EUNSUPPORTED, "fp8 on CUDA cores supports sq*num_heads/num_kv_heads <= 8 (got %d)", M);
         pl.mma = false;
@@ -118,6 +128,20 @@ pkd_status make_plan(int B, int sq, int Hq, int Hkv, int D, int P, int max_kv_le
     const long long span = window > 0 ? (long long)window + sq - 1 + P - 1 : (long long)max_kv_len;
     pl.max_vis = (int)(span < max_kv_len ? span : max_kv_len);
     const int units = B * Hkv > 0 ? B * Hkv : 1;
+    if (pl.tc) {
+        // work items of at most `chunk` keys (equal chunks within a request);
+        // each split unit keeps one partial slot of 32 rows per chunk
+        if (chunk_tokens > 0 && chunk_tokens % P != 0)
+            return fail(PKD_EINVAL, "chunk_tokens %d must be a multiple of page_size %d", chunk_tokens, P);
+        pl.chunk = chunk_tokens > 0 ? chunk_tokens : kTcChunk;
+        pl.max_splits = pl.max_vis > 0 ? (pl.max_vis + pl.chunk - 1) / pl.chunk : 1;
+        const size_t parts = (size_t)units * pl.max_splits;
+        pl.off_counters = kHeader;
+        pl.off_lse = pl.off_counters + round_up((size_t)units * 4, 256);
+        pl.off_out = pl.off_lse + round_up(parts * pkd::kTcRows * 4, 256);
+        pl.bytes = pl.off_out + round_up(parts * pkd::kTcRows * 128 * 4, 256);
+        return PKD_OK;
+    }
     if (chunk_tokens > 0) {
         if (chunk_tokens % P != 0)
             return fail(PKD_EINVAL, "chunk_tokens %d must be a multiple of page_size %d", chunk_tokens, P);
@@ -243,13 +267,17 @@ pkd_status get_map(CUtensorMap& out, const void* base, int rank, uint64_t d0, ui
 // so one TMA copy loads a 16-key stage (K and V) chunk-major.  With
 // half_rows the box is {one chunk, 8 rows, one chunk}: one copy per chunk
 // fills the first 8 rows of that chunk's 16-row slot.
+// Boxes of the stage map: a whole 16-key stage (every chunk), its first 8
+// rows of one chunk, or 8 rows of every chunk (a 4 KB group of K and V).
+enum StageBox { kStageFull = 0, kStageHalfRows = 1, kStageGroup8 = 2 };
+
 pkd_status get_stage_map(CUtensorMap& out, const void* cache, uint64_t rows, int row_bytes, pkd_dtype dt,
-                         bool half_rows = false) {
+                         StageBox mode = kStageFull) {
     const int elt = elt_bytes(dt);
     MapKey k;
     std::memset(&k, 0, sizeof k);
     k.base = cache; k.d0 = 128 / elt; k.d1 = rows; k.d2 = row_bytes / 128; k.s1 = row_bytes; k.s2 = 128;
-    k.rank = half_rows ? 108 : 103; k.dtype = dt;
+    k.rank = mode == kStageHalfRows ? 108 : mode == kStageGroup8 ? 120 : 103; k.dtype = dt;
     MapCache& c = map_cache();
     {
         std::lock_guard<std::mutex> g(c.mu);
@@ -266,13 +294,51 @@ pkd_status get_stage_map(CUtensorMap& out, const void* cache, uint64_t rows, int
                                                    : CU_TENSOR_MAP_DATA_TYPE_UINT8;
     cuuint64_t dims[3] = {k.d0, k.d1, k.d2};
     cuuint64_t strides[2] = {k.s1, k.s2};
-    cuuint32_t box[3] = {(cuuint32_t)(128 / elt), (cuuint32_t)(half_rows ? pkd::kStageTok / 2 : pkd::kStageTok),
-                         (cuuint32_t)(half_rows ? 1 : row_bytes / 128)};
+    cuuint32_t box[3] = {(cuuint32_t)(128 / elt), (cuuint32_t)(mode == kStageFull ? pkd::kStageTok : pkd::kStageTok / 2),
+                         (cuuint32_t)(mode == kStageHalfRows ? 1 : row_bytes / 128)};
     cuuint32_t estr[3] = {1, 1, 1};
     CUtensorMap m;
     CUresult r = enc(&m, t, 3, const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(PKD_ECUDA, "cuTensorMapEncodeTiled (stage map) failed (CUresult %d)", (int)r);
+    {
+        std::lock_guard<std::mutex> g(c.mu);
+        const int slot = c.used < MapCache::N ? c.used++ : (c.next++ % MapCache::N);
+        c.key[slot] = k;
+        c.map[slot] = m;
+    }
+    out = m;
+    return PKD_OK;
+}
+
+// The q rows of one (request, kv head) as a TMA box: q [tokens, Hq, D] viewed
+// as {D, Hq, tokens}, box {64 dims, G heads, sq tokens}, 128-byte swizzle, so
+// that one copy lands 64 dims of rows r = i*G + g at 128 bytes per row.
+pkd_status get_q_map(CUtensorMap& out, const void* q, int D, int Hq, uint64_t tokens, int G, int sq, pkd_dtype dt) {
+    MapKey k;
+    std::memset(&k, 0, sizeof k);
+    k.base = q; k.d0 = (uint64_t)D; k.d1 = (uint64_t)Hq; k.d2 = tokens; k.s1 = (uint64_t)D * 2;
+    k.s2 = (uint64_t)Hq * D * 2; k.rank = 1000 + G * 64 + sq; k.dtype = dt;
+    MapCache& c = map_cache();
+    {
+        std::lock_guard<std::mutex> g(c.mu);
+        for (int i = 0; i < c.used; ++i)
+            if (c.key[i] == k) {
+                out = c.map[i];
+                return PKD_OK;
+            }
+    }
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return fail(PKD_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const CUtensorMapDataType t = dt == PKD_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    cuuint64_t dims[3] = {k.d0, k.d1, k.d2};
+    cuuint64_t strides[2] = {k.s1, k.s2};
+    cuuint32_t box[3] = {64u, (cuuint32_t)G, (cuuint32_t)sq};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUtensorMap m;
+    CUresult r = enc(&m, t, 3, const_cast<void*>(q), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PKD_ECUDA, "cuTensorMapEncodeTiled (q map) failed (CUresult %d)", (int)r);
     {
         std::lock_guard<std::mutex> g(c.mu);
         const int slot = c.used < MapCache::N ? c.used++ : (c.next++ % MapCache::N);
@@ -318,6 +384,7 @@ const char* pkd_paged_decode_kernel_name(int batch, int sq, int num_heads, int n
     if (make_plan(batch, sq, num_heads, num_kv_heads, head_dim, page_size, max_kv_len, kv_dtype, window,
                   chunk_tokens, flags, pl) != PKD_OK)
         return nullptr;
+    if (pl.tc) return "persistent tcgen05 kernel, TMEM accumulators";
     if (pl.bal) return "persistent per-CTA partition, tensor cores";
     if (pl.flat) return pl.mma ? "persistent flat partition, tensor cores" : "persistent flat partition, CUDA cores";
     return pl.mma ? "chunked grid, tensor cores" : "chunked grid, CUDA cores";
@@ -418,7 +485,15 @@ pkd_status pkd_paged_decode(const void* q, pkd_dtype q_dtype, const void* kv_cac
     cudaError_t e;
     cudaStream_t s = (cudaStream_t)stream;
     const int max_ctas = pkd::kFlatMaxWorkers / pkd::kNW;
-    if (pl.bal)
+    if (pl.tc) {
+        CUtensorMap kvmap, qmap;
+        st = get_stage_map(kvmap, kv_cache, rows, 2 * head_dim * elt, kv_dtype, kStageGroup8);
+        if (st != PKD_OK) return st;
+        st = get_q_map(qmap, q, head_dim, num_heads, (uint64_t)batch * sq, pl.G, sq, kv_dtype);
+        if (st != PKD_OK) return st;
+        p.sched = reinterpret_cast<int32_t*>(ws + 64);
+        e = pkd::launch_decode_tc05(kv_dtype == PKD_BF16, kvmap, qmap, p, s);
+    } else if (pl.bal)
         e = pkd::launch_decode_bal(head_dim, kv_dtype == PKD_BF16, pl.mt, pl.nt, tmap, p, s);
     else if (pl.flat && pl.mma)
         e = kv_dtype == PKD_BF16   ? pkd::launch_flat_mma_bf16(head_dim, pl.mt, pl.nt, tmap, p, max_ctas, s)
@@ -560,7 +635,7 @@ pkd_status pkd_segmented_attention_paged(const void* q, pkd_dtype dtype, const v
     const uint64_t rows = (uint64_t)num_pages * num_kv_heads * page_size;
     pkd_status st = get_stage_map(p.kmap, kv_cache, rows, 4 * head_dim, dtype);
     if (st != PKD_OK) return st;
-    st = get_stage_map(p.vmap, kv_cache, rows, 4 * head_dim, dtype, true);  // stages whose keys end in 8 rows
+    st = get_stage_map(p.vmap, kv_cache, rows, 4 * head_dim, dtype, kStageHalfRows);  // stages whose keys end in 8 rows
     if (st != PKD_OK) return st;
     p.paged = 1;
     page_magic(page_size, p.pmagic, p.pmshift);

@@ -1,0 +1,655 @@
+// Paged decode of query blocks with 17-32 rows per kv head (M = sq * Hq/Hkv)
+// on the 5th-generation tensor cores, accumulators in tensor memory (TMEM).
+//
+// One persistent CTA per SM takes work items -- (request, chunk of keys, kv
+// head) -- from a queue in the workspace, so SMs that finish early take more.
+// Per 128-key tile of an item:
+//   S^T = K Q^T      tcgen05.mma, M = 128 keys, N = 32 query rows, K = 128
+//                    dims: A = the K tile as TMA lands it (K-major, 128-byte
+//                    swizzle), B = the item's q rows (K-major); S^T in TMEM.
+//   softmax          one key per thread of a warp group (TMEM lane = key):
+//                    tcgen05.ld of its 32 scores, online softmax per query
+//                    row in fp32 whose reference maximum moves only when a
+//                    row's maximum grows by more than 2^8 (then O and l are
+//                    rescaled), P written to shared memory in the operand
+//                    type.
+//   O^T += V^T P^T   M = 128 dims, N = 32 rows, K = 128 keys: A = the V tile
+//                    read MN-major, B = P (K-major); O^T accumulates in TMEM
+//                    over the item's tiles.
+// A tile lands as sixteen 4 KB groups of 8 keys, one TMA copy each, every
+// group holding the four 128-byte chunks of its rows (K dims 0-63, K 64-127,
+// V 0-63, V 64-127; 1 KB each, 128-byte swizzle): both products then see
+// rows at a uniform 4 KB stride, and a 16-key stage takes two copies.
+// Warp roles: warps 0-3 run the softmax, warps 4-7 the epilogue (read O^T,
+// normalise, write out and LSE -- or, for a request split into several
+// chunks, write the chunk's partial result), warp 8 loads (the item's
+// block-table entries, q per item, the K/V tiles), warp 9 issues the MMAs
+// (one thread).  The partials of split requests are merged by LSE in a
+// second, short kernel (decode_tc05.cu) launched right after on the same
+// stream: merging inside the persistent kernel left its epilogue warps
+// waiting on chains of L2 round trips at full HBM load.
+// Every wait is bounded; a failure raises the status word and every role
+// leaves after letting its own copies and products complete.
+#pragma once
+
+#include "decode_common.cuh"
+#include "tc05.cuh"
+
+namespace pkd {
+
+constexpr int kTcTile = 128;      // keys per tile: the M of S^T = K Q^T
+constexpr int kTcRows = 32;       // query rows per unit, padded: the N of both products
+constexpr int kTcNS = 3;          // K/V tile ring
+constexpr int kTcNI = 4;          // work-item ring
+constexpr int kTcMaxChunk = 2048; // keys per work item at most
+constexpr int kTcItemPages = kTcMaxChunk / kStageTok + 8;
+constexpr int kTcMaxBatch = 512;  // requests whose lengths and item counts the CTA keeps in shared memory
+constexpr int kTcPageRegs = (kTcItemPages + 31) / 32;  // block-table entries of an item per producer lane
+constexpr int kTcThreads = 320;   // softmax, epilogue (four warps each), loads, MMAs
+constexpr float kTcRescale = 8.f; // log2 units: P stays below 2^8 between rescales
+
+struct TcItem {
+    int b, hk, c, nch, t0, t1, ntiles, bad, end, pad[7];
+    int pages[kTcItemPages];      // table columns t0/P ..; -1: outside the pool (keys skipped)
+};
+
+// Shared memory.  Operand regions are 1024-byte aligned (128-byte swizzle atoms).
+struct TcShape {
+    static constexpr int GROUP = 4096;                 // 8 keys: K 0-63 | K 64-127 | V 0-63 | V 64-127
+    static constexpr int TILE = (kTcTile / 8) * GROUP; // 64 KB
+    static constexpr int QB = kTcRows * 256;           // q rows: two regions of 32 x 128 bytes
+    static constexpr int PB = kTcRows * kTcTile * 2;   // P: keys 0-63, then 64-127, 32 rows each
+    static constexpr int OFF_KV = 0;
+    static constexpr int OFF_Q = OFF_KV + kTcNS * TILE;
+    static constexpr int OFF_P = OFF_Q + 2 * QB;
+    static constexpr int OFF_ITEM = OFF_P + PB;
+    static constexpr int OFF_STAT = OFF_ITEM + kTcNI * static_cast<int>(sizeof(TcItem));  // [2][4 warps + m][32]
+    static constexpr int OFF_RED = OFF_STAT + 2 * 5 * kTcRows * 4;  // float [2][32 rows][4 warps]
+    static constexpr int OFF_VOTE = OFF_RED + 2 * kTcRows * 4 * 4;  // int votes [2][4] per group, merge flag
+    static constexpr int OFF_PREF = OFF_VOTE + 128;                 // int [kTcMaxBatch + 1]
+    static constexpr int OFF_LENS = OFF_PREF + (kTcMaxBatch + 1) * 4;  // int [kTcMaxBatch]: clamped lengths
+    static constexpr int OFF_BAR = (OFF_LENS + kTcMaxBatch * 4 + 7) & ~7;
+    // barriers: K/V full/empty, q full/empty, S full/empty, P full, P.V done,
+    // O full/free, stats full/free, item full/empty, final drain
+    static constexpr int B_TF = 0, B_TE = B_TF + kTcNS, B_QF = B_TE + kTcNS, B_QE = B_QF + 2;
+    static constexpr int B_SF = B_QE + 2, B_SE = B_SF + 2, B_PF = B_SE + 2, B_PD = B_PF + 1;
+    static constexpr int B_OF = B_PD + 1, B_OE = B_OF + 2, B_XF = B_OE + 2, B_XE = B_XF + 2;
+    static constexpr int B_IF = B_XE + 2, B_IE = B_IF + kTcNI, B_DR = B_IE + kTcNI, NBAR = B_DR + 1;
+    static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
+    static constexpr int SMEM = OFF_TMEM + 16 + 1024;
+    static_assert(SMEM <= 227 * 1024, "shared memory of one CTA");
+    static_assert(SMEM > 114 * 1024, "one CTA per SM: its 128 TMEM columns are always free");
+};
+
+// Row reduction of a warp's 32 keys: each lane holds v[r] for its key and
+// rows r = 0..31; returns, in lane r, op over the warp's keys of row r.
+// (At each step the lane keeps the half of its rows whose index bit matches
+// its own lane bit and receives its partner's values for them.)
+template <class Op>
+__device__ __forceinline__ float tc_row_reduce(const float (&v)[32], int lane, Op op) {
+    float a[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const bool up = lane & 16;
+        a[i] = op(up ? v[i + 16] : v[i], __shfl_xor_sync(kFull, up ? v[i] : v[i + 16], 16));
+    }
+    float b[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const bool up = lane & 8;
+        b[i] = op(up ? a[i + 8] : a[i], __shfl_xor_sync(kFull, up ? a[i] : a[i + 8], 8));
+    }
+    float c[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const bool up = lane & 4;
+        c[i] = op(up ? b[i + 4] : b[i], __shfl_xor_sync(kFull, up ? b[i] : b[i + 4], 4));
+    }
+    float d[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const bool up = lane & 2;
+        d[i] = op(up ? c[i + 2] : c[i], __shfl_xor_sync(kFull, up ? c[i] : c[i + 2], 2));
+    }
+    const bool up = lane & 1;
+    return op(up ? d[1] : d[0], __shfl_xor_sync(kFull, up ? d[0] : d[1], 1));
+}
+
+// A four-warp group's own barrier: named barrier `id`, 128 threads.
+__device__ __forceinline__ void tc_group_sync(int id) { asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory"); }
+
+// A vote of a four-warp group: OR of `bits` over the group.  Votes alternate
+// between two buffers: a warp writes buffer v only after the barrier of vote
+// v - 1, which every warp passes after reading vote v - 2.
+__device__ __forceinline__ int tc_vote(int* votes, int id, int& nvote, int q4, int lane, int bits) {
+    bits = __reduce_or_sync(kFull, bits);
+    int* v = votes + (nvote & 1) * 4;
+    ++nvote;
+    if (lane == 0) v[q4] = bits;
+    tc_group_sync(id);
+    return v[0] | v[1] | v[2] | v[3];
+}
+
+// A wait every lane of the warp takes, with a warp-uniform result.
+__device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity, const DecodeParams& p, uint64_t limit) {
+    return __all_sync(kFull, mbar_wait(bar, parity, p.status, limit));
+}
+
+// Element r of a register array, r not known at compile time (no local memory).
+__device__ __forceinline__ float tc_pick(const float (&v)[32], int r) {
+    float x = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) x = i == r ? v[i] : x;
+    return x;
+}
+
+template <bool kBF16>
+__global__ void __launch_bounds__(kTcThreads, 1)
+decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_constant__ CUtensorMap qmap,
+                   const DecodeParams p) {
+    using S = TcShape;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb0 = smem_u32(smem);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::OFF_BAR);
+    TcItem* items = reinterpret_cast<TcItem*>(smem + S::OFF_ITEM);
+    float* stats = reinterpret_cast<float*>(smem + S::OFF_STAT);
+    float* red = reinterpret_cast<float*>(smem + S::OFF_RED);
+    int* votes = reinterpret_cast<int*>(smem + S::OFF_VOTE);
+    int* pref = reinterpret_cast<int*>(smem + S::OFF_PREF);
+    int* lens = reinterpret_cast<int*>(smem + S::OFF_LENS);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + S::OFF_TMEM);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int Hkv = p.Hkv, M = p.M, C = p.chunk;
+    auto bar = [&](int i) { return smem_u32(bars + i); };
+
+    // ------------------------------------------------------------ set-up
+    if (tid == 0) {
+        for (int i = 0; i < kTcNS; ++i) {
+            mbar_init(bar(S::B_TF + i), 1);
+            mbar_init(bar(S::B_TE + i), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(S::B_QF + i), 1);
+            mbar_init(bar(S::B_QE + i), 1);
+            mbar_init(bar(S::B_SF + i), 1);
+            mbar_init(bar(S::B_SE + i), 128);
+            mbar_init(bar(S::B_OF + i), 1);
+            mbar_init(bar(S::B_OE + i), 128);
+            mbar_init(bar(S::B_XF + i), 128);
+            mbar_init(bar(S::B_XE + i), 128);
+        }
+        mbar_init(bar(S::B_PF), 128);
+        mbar_init(bar(S::B_PD), 1);
+        for (int i = 0; i < kTcNI; ++i) {
+            mbar_init(bar(S::B_IF + i), 32);
+            mbar_init(bar(S::B_IE + i), 1 + 128 + 128);  // the MMA thread, softmax and epilogue groups
+        }
+        mbar_init(bar(S::B_DR), 1);
+        fence_barrier_init();
+    }
+    if (warp == 9) {
+        tc05::alloc(smem_u32(tslot), 128);  // S^T: columns 0-63 (two buffers), O^T: 64-127 (two)
+        tc05::relinquish_alloc_permit();
+    }
+    if (warp == 8) {
+        // work items per request (chunks x kv heads), prefix in pref[0..B]
+        int run = 0;
+        for (int b0 = 0; b0 < p.B; b0 += 32) {
+            const int b = b0 + lane;
+            int n = 0;
+            if (b < p.B) {
+                const int L = clamp_len(p, b, true), vis = L - visible_lo(p, L);
+                n = vis > 0 ? (vis + C - 1) / C * Hkv : 0;
+                lens[b] = L;
+            }
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(kFull, n, o);
+                if (lane >= o) n += y;
+            }
+            if (b < p.B) pref[b + 1] = run + n;
+            run += __shfl_sync(kFull, n, 31);
+        }
+        if (lane == 0) pref[0] = 0;
+    }
+    if (warp < 4 && M < kTcRows) {
+        // q rows M..31 of both buffers stay zero (the copies fill rows < M)
+        for (int e = tid; e < 2 * 2 * (kTcRows - M) * 8; e += 128) {
+            const int chunk = e & 7, row = M + (e >> 3) % (kTcRows - M), reg = (e >> 3) / (kTcRows - M);
+            *reinterpret_cast<uint4*>(smem + S::OFF_Q + reg * 4096 + row * 128 + chunk * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async();
+    }
+    if (warp >= 4 && warp < 8) {
+        // requests without a visible key: out = 0, lse = -inf
+        const int et = tid - 128;
+        for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
+            const int L = clamp_len(p, b, false);
+            if (L - visible_lo(p, L) > 0) continue;
+            for (int e = et; e < Hkv * M * 128; e += 128) {
+                const int hk = e / (M * 128), r = (e / 128) % M, d = e % 128;
+                store_out(p.out, out_index(p, b, hk, r, d, 128), 0.f, p.out_dtype);
+                if (d == 0 && p.lse)
+                    p.lse[(static_cast<long long>(b) * p.sq + r / p.G) * p.Hq + hk * p.G + r % p.G] = -INFINITY;
+            }
+        }
+    }
+    tc05::fence_before_sync();
+    __syncthreads();
+    tc05::fence_after_sync();
+    const uint32_t tmem = *tslot;
+    const int n_items = pref[p.B];
+    constexpr uint32_t kIdS = tc05::idesc_f16(kBF16, kTcTile, kTcRows, false, false);  // S^T = K Q^T
+    constexpr uint32_t kIdO = tc05::idesc_f16(kBF16, kTcTile, kTcRows, true, false);   // O^T += V^T P^T
+
+    if (warp == 8) {
+        // ---------------------------------------------------------- loads
+        const uint64_t pol = policy_evict_first();
+        if (lane == 0) {
+            prefetch_tmap(&kvmap);
+            prefetch_tmap(&qmap);
+        }
+        int t = 0, tiss = 0, qiss = 0, nxt = 0;
+        bool ok = true;
+        // Work item i: its request, chunk and kv head, and the block-table
+        // entries of its keys, loaded one item ahead into registers (lane j
+        // holds entries j, j + 32, ...) so that they have landed when the item
+        // is published.
+        struct Work {
+            int i, b, hk, c, nch, t0, t1, ntiles, col0, npg;
+        };
+        auto decode = [&](int i, Work& x) {
+            x.i = i;
+            if (i >= n_items) return;
+            int lo_b = 0, hi_b = p.B;  // pref[lo_b] <= i < pref[hi_b]
+            while (hi_b - lo_b > 1) {
+                const int mid = (lo_b + hi_b) >> 1;
+                if (pref[mid] <= i) lo_b = mid; else hi_b = mid;
+            }
+            const int L = lens[lo_b], lo = visible_lo(p, L), vis = L - lo, rem = i - pref[lo_b];
+            x.b = lo_b;
+            x.c = rem / Hkv;
+            x.hk = rem - x.c * Hkv;
+            x.nch = (vis + C - 1) / C;
+            const int cb = ((vis + x.nch - 1) / x.nch + kStageTok - 1) & ~(kStageTok - 1);  // equal chunks, whole stages
+            x.t0 = lo + x.c * cb;
+            x.t1 = min(x.t0 + cb, L);
+            x.ntiles = (x.t1 - x.t0 + kTcTile - 1) / kTcTile;
+            x.col0 = page_div(x.t0, p.pmagic, p.pmshift);
+            x.npg = page_div(x.t1 - 1, p.pmagic, p.pmshift) - x.col0 + 1;
+        };
+        int pg_next[kTcPageRegs];
+        auto load_pages = [&](const Work& x) {
+#pragma unroll
+            for (int k = 0; k < kTcPageRegs; ++k) {
+                const int j = lane + 32 * k;
+                pg_next[k] = (x.i < n_items && j < x.npg)
+                                 ? p.block_table[static_cast<long long>(x.b) * p.bt_stride + x.col0 + j] : -1;
+            }
+        };
+        if (lane == 0) nxt = atomicAdd(p.sched, 1);
+        Work w;
+        decode(__shfl_sync(kFull, nxt, 0), w);
+        load_pages(w);
+        if (lane == 0) nxt = atomicAdd(p.sched, 1);
+        for (int it = 0;; ++it) {
+            const int slot = it % kTcNI;
+            if (it >= kTcNI && !tc_wait(bar(S::B_IE + slot), ((it / kTcNI) - 1) & 1, p, kWaitNs)) { ok = false; break; }
+            TcItem& I = items[slot];
+            if (w.i >= n_items) {
+                if (lane == 0) I.end = 1;
+                __syncwarp();
+                mbar_arrive(bar(S::B_IF + slot));
+                break;
+            }
+            const int b = w.b, hk = w.hk, t0 = w.t0, t1 = w.t1, ntiles = w.ntiles, col0 = w.col0;
+            int bad = 0;
+#pragma unroll
+            for (int k = 0; k < kTcPageRegs; ++k) {
+                const int j = lane + 32 * k;
+                if (j < w.npg) {
+                    int pg = pg_next[k];
+                    if (pg < 0 || pg >= p.num_pages) {
+                        raise_status(p, kErrBounds);
+                        pg = -1;
+                        bad = 1;
+                    }
+                    I.pages[j] = pg;
+                }
+            }
+            bad = __any_sync(kFull, bad);
+            if (lane == 0) {
+                I.b = b; I.hk = hk; I.c = w.c; I.nch = w.nch; I.t0 = t0; I.t1 = t1; I.ntiles = ntiles; I.bad = bad;
+                I.end = 0;
+            }
+            __syncwarp();
+            mbar_arrive(bar(S::B_IF + slot));
+            // the next item, decoded and its table entries requested while this one streams
+            decode(__shfl_sync(kFull, nxt, 0), w);
+            load_pages(w);
+            if (lane == 0) nxt = atomicAdd(p.sched, 1);
+            // the unit's q rows (two 64-dim halves)
+            const int qb = it & 1;
+            if (it >= 2 && !tc_wait(bar(S::B_QE + qb), ((it >> 1) - 1) & 1, p, kWaitNs)) { ok = false; break; }
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar(S::B_QF + qb), M * 256);
+                for (int h = 0; h < 2; ++h)
+                    tma_load_3d(sb0 + S::OFF_Q + qb * S::QB + h * 4096, &qmap, 64 * h, hk * p.G, b * p.sq,
+                                bar(S::B_QF + qb), pol);
+            }
+            ++qiss;
+            // K/V tiles: lane s < 8 loads stage s (two 8-key groups, 4 KB each)
+            for (int k = 0; k < ntiles; ++k, ++t) {
+                const int tok0 = t0 + k * kTcTile, ts = t % kTcNS;
+                if (t >= kTcNS && !tc_wait(bar(S::B_TE + ts), ((t / kTcNS) - 1) & 1, p, kWaitNs)) { ok = false; break; }
+                const int tok = tok0 + lane * kStageTok;
+                const int col = page_div(tok, p.pmagic, p.pmshift);
+                const int pg = (lane < kTcTile / kStageTok && tok < t1) ? I.pages[col - col0] : -1;
+                const unsigned loaded = __ballot_sync(kFull, pg >= 0);
+                if (lane == 0) mbar_arrive_expect_tx(bar(S::B_TF + ts), __popc(loaded) * 2 * S::GROUP);
+                __syncwarp();
+                if (pg >= 0) {
+                    const int row = (pg * Hkv + hk) * p.P + (tok - col * p.P);
+                    const uint32_t dst = sb0 + S::OFF_KV + ts * S::TILE + 2 * lane * S::GROUP;
+                    tma_load_3d(dst, &kvmap, 0, row, 0, bar(S::B_TF + ts), pol);
+                    tma_load_3d(dst + S::GROUP, &kvmap, 0, row + 8, 0, bar(S::B_TF + ts), pol);
+                }
+                ++tiss;
+            }
+            if (!ok) break;
+        }
+        if (!ok) {
+            // let every issued copy land before the CTA leaves
+            if (lane == 0) raise_status(p, kErrTimeout);
+            for (int j = max(0, tiss - kTcNS); j < tiss; ++j) mbar_wait(bar(S::B_TF + j % kTcNS), (j / kTcNS) & 1);
+            for (int j = max(0, qiss - 2); j < qiss; ++j) mbar_wait(bar(S::B_QF + (j & 1)), (j >> 1) & 1);
+        }
+    } else if (warp == 9) {
+        // ----------------------------------------------------------- MMAs
+        if (lane == 0) {
+            bool ok = true, have = false;
+            int t = 0, pt = 0, pit = 0, pfirst = 0, plast = 0;  // the tile whose O^T += V^T P^T is pending
+            auto issue_pv = [&]() -> bool {
+                const int ts = pt % kTcNS, ob = pit & 1;
+                if (!mbar_wait(bar(S::B_PF), pt & 1, p.status)) return false;
+                if (pfirst && pit >= 2 && !mbar_wait(bar(S::B_OE + ob), ((pit >> 1) - 1) & 1, p.status)) return false;
+                tc05::fence_after_sync();
+                const uint32_t tile = sb0 + S::OFF_KV + ts * S::TILE, ptile = sb0 + S::OFF_P;
+#pragma unroll
+                for (int j = 0; j < kTcTile / 16; ++j)
+                    tc05::mma_f16(tmem + 64 + 32 * ob, tc05::smem_desc(tile + 2 * j * S::GROUP + 2048, 1024, S::GROUP),
+                                  tc05::smem_desc(ptile + (j >> 2) * 4096 + (j & 3) * 32, 16, 1024), kIdO,
+                                  !(pfirst && j == 0));
+                tc05::commit(bar(S::B_PD));
+                tc05::commit(bar(S::B_TE + ts));
+                if (plast) tc05::commit(bar(S::B_OF + ob));
+                return true;
+            };
+            for (int it = 0; ok; ++it) {
+                const int slot = it % kTcNI;
+                if (!mbar_wait(bar(S::B_IF + slot), (it / kTcNI) & 1, p.status)) { ok = false; break; }
+                const TcItem& I = items[slot];
+                if (I.end) break;
+                const int ntiles = I.ntiles, qb = it & 1;
+                mbar_arrive(bar(S::B_IE + slot));
+                if (!mbar_wait(bar(S::B_QF + qb), (it >> 1) & 1, p.status, p.wait_ns)) { ok = false; break; }
+                for (int k = 0; k < ntiles; ++k, ++t) {
+                    const int ts = t % kTcNS, sbuf = t & 1;
+                    if (!mbar_wait(bar(S::B_TF + ts), (t / kTcNS) & 1, p.status, p.wait_ns)) { ok = false; break; }
+                    if (t >= 2 && !mbar_wait(bar(S::B_SE + sbuf), ((t >> 1) - 1) & 1, p.status)) { ok = false; break; }
+                    tc05::fence_after_sync();
+                    const uint32_t tile = sb0 + S::OFF_KV + ts * S::TILE, qt = sb0 + S::OFF_Q + qb * S::QB;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        tc05::mma_f16(tmem + 32 * sbuf,
+                                      tc05::smem_desc(tile + (kk >> 2) * 1024 + (kk & 3) * 32, 16, S::GROUP),
+                                      tc05::smem_desc(qt + (kk >> 2) * 4096 + (kk & 3) * 32, 16, 1024), kIdS, kk > 0);
+                    tc05::commit(bar(S::B_SF + sbuf));
+                    if (k == ntiles - 1) tc05::commit(bar(S::B_QE + qb));
+                    if (have && !issue_pv()) { ok = false; break; }
+                    pt = t;
+                    pit = it;
+                    pfirst = k == 0;
+                    plast = k == ntiles - 1;
+                    have = true;
+                }
+            }
+            if (ok && have) ok = issue_pv();
+            if (!ok) raise_status(p, kErrTimeout);
+            // every product issued has completed before TMEM is freed
+            tc05::commit(bar(S::B_DR));
+            mbar_wait(bar(S::B_DR), 0);
+        }
+        __syncwarp();
+    } else if (warp < 4) {
+        // ------------------------------------------------------- softmax
+        const int q4 = warp, key = 32 * q4 + lane;   // TMEM lane of S^T
+        const uint32_t lane_addr = static_cast<uint32_t>(32 * q4) << 16;
+        const float scale2 = p.scale_log2;
+        int nvote = 0, t = 0;
+        float m_used[32], lp[32];
+        for (int it = 0;; ++it) {
+            const int slot = it % kTcNI, ob = it & 1;
+            const int fail = !tc_wait(bar(S::B_IF + slot), (it / kTcNI) & 1, p, kWaitNs);
+            const TcItem& I = items[slot];
+            const int end = fail ? 1 : I.end;
+            if (tc_vote(votes, 1, nvote, q4, lane, (fail ? 2 : 0) | (end ? 1 : 0))) {
+                if (fail) raise_status(p, kErrTimeout);
+                break;
+            }
+            const int t0 = I.t0, t1 = I.t1, ntiles = I.ntiles, bad = I.bad;
+            const int col0 = page_div(t0, p.pmagic, p.pmshift);
+#pragma unroll
+            for (int r = 0; r < 32; ++r) {
+                m_used[r] = -INFINITY;
+                lp[r] = 0.f;
+            }
+            bool abort = false;
+            for (int k = 0; k < ntiles; ++k, ++t) {
+                const int sbuf = t & 1, ts = t % kTcNS;
+                const int tok0 = t0 + k * kTcTile;
+                const int nvalid = min(kTcTile, t1 - tok0);
+                bool valid = key < nvalid;
+                if (bad && valid) valid = I.pages[page_div(tok0 + key, p.pmagic, p.pmshift) - col0] >= 0;
+                float x[32];
+                const bool got = tc_wait(bar(S::B_SF + sbuf), (t >> 1) & 1, p, kWaitNs);
+                if (got) {
+                    tc05::fence_after_sync();
+                    uint32_t sr[32];
+                    tc05::ld_32x32b_x32(tmem + lane_addr + 32 * sbuf, sr);
+                    tc05::wait_ld();
+                    tc05::fence_before_sync();
+                    mbar_arrive(bar(S::B_SE + sbuf));
+#pragma unroll
+                    for (int r = 0; r < 32; ++r) x[r] = (valid && r < M) ? __uint_as_float(sr[r]) * scale2 : -INFINITY;
+                } else {
+#pragma unroll
+                    for (int r = 0; r < 32; ++r) x[r] = -INFINITY;
+                }
+                int need = 0;
+#pragma unroll
+                for (int r = 0; r < 32; ++r) need |= x[r] > m_used[r] + kTcRescale;
+                const int v = tc_vote(votes, 1, nvote, q4, lane, (got ? 0 : 2) | need);
+                if (v & 2) {
+                    raise_status(p, kErrTimeout);
+                    abort = true;
+                    break;
+                }
+                if (v & 1) {
+                    // a row's maximum grew past the reference: new references from
+                    // the tile's row maxima, and O and l rescaled to them
+                    // lane r works out row r's new reference and factor, then
+                    // every lane takes them by shuffle
+                    float* rb = red + (nvote & 1) * kTcRows * 4;
+                    const float y = tc_row_reduce(x, lane, [](float a, float b2) { return fmaxf(a, b2); });
+                    rb[lane * 4 + q4] = y;
+                    tc_group_sync(1);
+                    const float4 w = *reinterpret_cast<const float4*>(rb + lane * 4);
+                    const float m_old = tc_pick(m_used, lane);
+                    const float m_new = fmaxf(m_old, fmaxf(fmaxf(w.x, w.y), fmaxf(w.z, w.w)));
+                    const float a_lane = m_new == m_old ? 1.f : fast_exp2(m_old - m_new);
+                    const bool grew = __any_sync(kFull, m_new > m_old);
+#pragma unroll
+                    for (int r = 0; r < 32; ++r) {
+                        m_used[r] = __shfl_sync(kFull, m_new, r);
+                        lp[r] *= __shfl_sync(kFull, a_lane, r);
+                    }
+                    if (grew && k > 0) {
+                        // O holds the item's earlier tiles: rescale once their P.V has completed
+                        if (tc_wait(bar(S::B_PD), (t - 1) & 1, p, kWaitNs)) {
+                            tc05::fence_after_sync();
+                            uint32_t o[32];
+                            tc05::ld_32x32b_x32(tmem + lane_addr + 64 + 32 * ob, o);
+                            tc05::wait_ld();
+#pragma unroll
+                            for (int r = 0; r < 32; ++r)
+                                o[r] = __float_as_uint(__uint_as_float(o[r]) * __shfl_sync(kFull, a_lane, r));
+                            tc05::st_32x32b_x32(tmem + lane_addr + 64 + 32 * ob, o);
+                            tc05::wait_st();
+                        } else {
+                            abort = true;  // reported at the next vote
+                        }
+                    }
+                }
+                // P (rows past M and keys outside the chunk are 0), once the previous
+                // tile's P.V has read the buffer
+                float pr[32];
+#pragma unroll
+                for (int r = 0; r < 32; ++r) {
+                    pr[r] = m_used[r] == -INFINITY ? 0.f : fast_exp2(x[r] - m_used[r]);
+                    lp[r] += pr[r];
+                }
+                if (t >= 1 && !tc_wait(bar(S::B_PD), (t - 1) & 1, p, kWaitNs)) abort = true;
+                uint8_t* ptile = smem + S::OFF_P + (key >> 6) * 4096;
+                const int kc = (key & 63) >> 3, kb2 = (key & 7) * 2;
+#pragma unroll
+                for (int r = 0; r < 32; ++r) {
+                    const uint32_t h = pack2<kBF16>(pr[r], 0.f);
+                    *reinterpret_cast<uint16_t*>(ptile + r * 128 + (((kc ^ (r & 7)) << 4) | kb2)) =
+                        static_cast<uint16_t>(h & 0xffffu);
+                }
+                if (__any_sync(kFull, !valid)) {
+                    // keys outside the chunk (or on a skipped page) get P = 0; their V
+                    // rows, stale or never loaded, are zeroed so that 0 * NaN cannot occur
+                    if (!tc_wait(bar(S::B_TF + ts), (t / kTcNS) & 1, p, kWaitNs)) abort = true;
+                    if (!valid) {
+                        uint8_t* vrow = smem + S::OFF_KV + ts * S::TILE + (key >> 3) * S::GROUP + 2048 + (key & 7) * 128;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            *reinterpret_cast<uint4*>(vrow + j * 16) = make_uint4(0, 0, 0, 0);
+                            *reinterpret_cast<uint4*>(vrow + 1024 + j * 16) = make_uint4(0, 0, 0, 0);
+                        }
+                    }
+                }
+                fence_proxy_async();      // P and zeroed rows are read by the tensor cores
+                tc05::fence_before_sync();
+                mbar_arrive(bar(S::B_PF));
+            }
+            if (tc_vote(votes, 1, nvote, q4, lane, abort ? 2 : 0) & 2) {
+                raise_status(p, kErrTimeout);
+                break;
+            }
+            // row statistics for the epilogue: this warp's share of l, and m
+            const float lw = tc_row_reduce(lp, lane, [](float a, float b2) { return a + b2; });
+            const bool free_ok = it < 2 || tc_wait(bar(S::B_XE + ob), ((it >> 1) - 1) & 1, p, kWaitNs);
+            float* st = stats + ob * 5 * kTcRows;
+            st[q4 * kTcRows + lane] = lw;
+            if (q4 == 0) st[4 * kTcRows + lane] = tc_pick(m_used, lane);
+            mbar_arrive(bar(S::B_XF + ob));
+            mbar_arrive(bar(S::B_IE + slot));
+            if (!free_ok) {
+                raise_status(p, kErrTimeout);  // the next vote stops the group
+            }
+        }
+    } else {
+        // ------------------------------------------------------ epilogue
+        const int q4 = warp - 4, et = tid - 128, d = 32 * q4 + lane;  // TMEM lane of O^T: the head dim
+        const uint32_t lane_addr = static_cast<uint32_t>(32 * q4) << 16;
+        int* evotes = votes + 8;
+        int nvote = 0;
+        for (int it = 0;; ++it) {
+            const int slot = it % kTcNI, ob = it & 1;
+            int fail = !tc_wait(bar(S::B_IF + slot), (it / kTcNI) & 1, p, kWaitNs);
+            const TcItem& I = items[slot];
+            const int end = fail ? 1 : I.end;
+            if (!end) {
+                fail |= !tc_wait(bar(S::B_XF + ob), (it >> 1) & 1, p, kWaitNs);
+                fail |= !tc_wait(bar(S::B_OF + ob), (it >> 1) & 1, p, kWaitNs);
+            }
+            if (tc_vote(evotes, 2, nvote, q4, lane, (fail ? 2 : 0) | (end ? 1 : 0))) {
+                if (fail) raise_status(p, kErrTimeout);
+                break;
+            }
+            const int b = I.b, hk = I.hk, c = I.c, nch = I.nch;
+            // O^T of the item (this thread's head dim, 32 rows); l and m per row
+            // are read from the softmax's statistics as they are needed
+            tc05::fence_after_sync();
+            uint32_t o[32];
+            tc05::ld_32x32b_x32(tmem + lane_addr + 64 + 32 * ob, o);
+            tc05::wait_ld();
+            tc05::fence_before_sync();
+            mbar_arrive(bar(S::B_OE + ob));
+            const float* st = stats + ob * 5 * kTcRows;
+            auto lrow = [&](int r) { return (st[r] + st[kTcRows + r]) + (st[2 * kTcRows + r] + st[3 * kTcRows + r]); };
+            const long long unit = static_cast<long long>(b) * Hkv + hk;
+            const long long row0 = static_cast<long long>(b) * p.sq * p.Hq + hk * p.G;  // output row of query row 0
+            auto out_row = [&](int r) { return row0 + static_cast<long long>(r / p.G) * p.Hq + r % p.G; };
+            if (nch == 1) {
+                int i = 0, g = 0;
+#pragma unroll
+                for (int r = 0; r < 32; ++r) {
+                    if (r >= M) break;
+                    const float l = lrow(r);
+                    store_out(p.out, (row0 + static_cast<long long>(i) * p.Hq + g) * 128 + d,
+                              l > 0.f ? __uint_as_float(o[r]) / l * p.v_scale : 0.f, p.out_dtype);
+                    if (++g == p.G) {
+                        g = 0;
+                        ++i;
+                    }
+                }
+                if (p.lse && d < M) {
+                    const float l = lrow(d);
+                    p.lse[out_row(d)] = l > 0.f ? (st[4 * kTcRows + d] + __log2f(l)) * kLn2 : -INFINITY;
+                }
+                mbar_arrive(bar(S::B_XE + ob));
+            } else {
+                // this chunk's partial (normalised O, LSE in log2 units), merged
+                // by the merge kernel after this launch
+                const long long slot2 = unit * p.max_splits + c;
+                float* po = p.part_out + slot2 * kTcRows * 128;
+#pragma unroll
+                for (int r = 0; r < 32; ++r) {
+                    if (r >= M) break;
+                    const float l = lrow(r);
+                    __stcg(po + r * 128 + d, l > 0.f ? __uint_as_float(o[r]) / l : 0.f);
+                }
+                if (d < M) {
+                    const float l = lrow(d);
+                    __stcg(p.part_lse + slot2 * kTcRows + d, l > 0.f ? st[4 * kTcRows + d] + __log2f(l) : -INFINITY);
+                }
+                mbar_arrive(bar(S::B_XE + ob));
+            }
+            mbar_arrive(bar(S::B_IE + slot));
+        }
+    }
+
+    // ---------------------------------------------------------- tear-down
+    tc05::fence_before_sync();
+    __syncthreads();
+    if (warp == 9) {
+        tc05::fence_after_sync();
+        tc05::dealloc(tmem, 128);
+    }
+    if (tid == 0) {
+        // the last CTA to finish resets the queue for the next call
+        __threadfence();
+        const int prev = atomicAdd(p.sched + 32, 1);
+        if (prev == static_cast<int>(gridDim.x) - 1) {
+            atomicExch(p.sched, 0);
+            atomicExch(p.sched + 32, 0);
+        }
+    }
+}
+
+}  // namespace pkd

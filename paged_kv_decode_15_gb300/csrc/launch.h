@@ -52,6 +52,12 @@ struct DecodeParams;
 // Launch one decode kernel variant on `stream`; grid = (max_splits, Hkv, B).
 cudaError_t launch_decode_mma(int D, bool bf16, int MT, int NT, const CUtensorMap& tmap,
                               const DecodeParams& p, dim3 grid, cudaStream_t stream);
+// Query blocks of 17-32 rows (16-bit caches, head_dim 128, no causal mask) on
+// tcgen05 tensor cores: persistent CTAs, one per SM, taking work items from a
+// queue.  kvmap: the stage map with boxes of 8 rows and every 128-byte chunk;
+// qmap: q as {dims, heads, tokens} with boxes {64, G, sq}.
+cudaError_t launch_decode_tc05(bool bf16, const CUtensorMap& kvmap, const CUtensorMap& qmap, const DecodeParams& p,
+                               cudaStream_t stream);
 // e4m3 caches on tensor cores in the chunked grid (M <= 16)
 cudaError_t launch_decode_mma_fp8(int D, int MT, int NT, const CUtensorMap& tmap, const DecodeParams& p, dim3 grid,
                                   cudaStream_t stream);

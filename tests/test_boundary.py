@@ -58,11 +58,17 @@ def test_workspace_plan_is_a_host_function(lib):
     # ... fp8 caches too ...
     assert pkd.workspace_size(64, 1, 32, 8, 128, 16, 4096, pkd.FP8_E4M3) == \
         pkd.workspace_size(64, 1, 32, 8, 128, 16, 4096, pkd.FP8_E4M3, flags=pkd.FLAG_GRID)
-    # ... 16-bit M > 16 too (warp pairs, as few chunks as the 4096-key limit allows:
-    # 8192 keys -> 2 chunks -> partials [512 units, 2, 32 rows, 128] fp32) ...
+    # ... 16-bit M > 16 without a causal mask takes the tcgen05 kernel: work
+    # items of at most 1024 keys, a partial slot of 32 rows per (unit, chunk) ...
     w = pkd.workspace_size(64, 8, 32, 8, 128, 16, 8192, pkd.BF16)
-    assert w == pkd.workspace_size(64, 8, 32, 8, 128, 16, 8192, pkd.BF16, chunk_tokens=4096, flags=pkd.FLAG_GRID)
-    assert 512 * 2 * 32 * 128 * 4 <= w < 512 * 3 * 32 * 128 * 4
+    assert 512 * 8 * 32 * 128 * 4 <= w < 512 * 9 * 32 * 128 * 4
+    assert w == pkd.workspace_size(64, 8, 32, 8, 128, 16, 8192, pkd.BF16, chunk_tokens=1024)
+    assert w > pkd.workspace_size(64, 8, 32, 8, 128, 16, 8192, pkd.BF16, chunk_tokens=2048)
+    # ... causal blocks and forced grids keep the warp-pair kernel (as few chunks
+    # as the 4096-key limit allows: 8192 keys -> 2 chunks -> partials [512, 2, 32, 128])
+    g = pkd.workspace_size(64, 8, 32, 8, 128, 16, 8192, pkd.BF16, flags=pkd.FLAG_CAUSAL)
+    assert g == pkd.workspace_size(64, 8, 32, 8, 128, 16, 8192, pkd.BF16, chunk_tokens=4096, flags=pkd.FLAG_GRID)
+    assert 512 * 2 * 32 * 128 * 4 <= g < 512 * 3 * 32 * 128 * 4
     # ... while fp8 with M > 16 stays on the flat partition whatever the lengths
     assert pkd.workspace_size(64, 8, 32, 8, 128, 16, 4096, pkd.FP8_E4M3) == \
         pkd.workspace_size(64, 8, 32, 8, 128, 16, 131072, pkd.FP8_E4M3)
@@ -157,7 +163,14 @@ def test_kernel_name_follows_the_plan(lib):
     assert pkd.kernel_name(*args, pkd.BF16) == "chunked grid, tensor cores"
     assert pkd.kernel_name(*args, pkd.BF16, flags=pkd.FLAG_FLAT) == "persistent flat partition, tensor cores"
     assert pkd.kernel_name(8, 1, 32, 8, 128, 16, 4096, pkd.BF16) == "chunked grid, tensor cores"
-    assert pkd.kernel_name(8, 8, 32, 8, 128, 16, 4096, pkd.BF16) == "chunked grid, tensor cores"
+    assert pkd.kernel_name(8, 8, 32, 8, 128, 16, 4096, pkd.BF16) == "persistent tcgen05 kernel, TMEM accumulators"
+    assert pkd.kernel_name(8, 8, 32, 8, 128, 16, 4096, pkd.FP16) == "persistent tcgen05 kernel, TMEM accumulators"
+    assert pkd.kernel_name(8, 8, 32, 8, 128, 16, 4096, pkd.BF16, flags=pkd.FLAG_CAUSAL) == "chunked grid, tensor cores"
+    assert pkd.kernel_name(8, 8, 32, 8, 128, 16, 4096, pkd.BF16, flags=pkd.FLAG_GRID) == "chunked grid, tensor cores"
+    assert pkd.kernel_name(8, 8, 32, 8, 64, 16, 4096, pkd.BF16) == "chunked grid, tensor cores"
+    assert pkd.kernel_name(8, 8, 32, 8, 128, 16, 8192, pkd.BF16, chunk_tokens=4096) == "chunked grid, tensor cores"
+    assert pkd.kernel_name(2048, 8, 32, 8, 128, 16, 4096, pkd.BF16) == "chunked grid, tensor cores"
+    assert pkd.kernel_name(513, 8, 32, 8, 128, 16, 4096, pkd.BF16) == "chunked grid, tensor cores"
     assert pkd.kernel_name(8, 8, 32, 8, 128, 16, 4096, pkd.FP8_E4M3) == "persistent flat partition, tensor cores"
     assert pkd.kernel_name(*args, pkd.BF16, flags=pkd.FLAG_FMA | pkd.FLAG_GRID) == "chunked grid, CUDA cores"
     assert pkd.kernel_name(*args, pkd.FP8_E4M3) == "chunked grid, tensor cores"
