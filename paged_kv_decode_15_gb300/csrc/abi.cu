@@ -49,7 +49,7 @@ constexpr int kMaxChunk = 4096;    // and never puts more keys than this in one 
 constexpr size_t kHeader = 256;    // workspace status word lives in the first bytes (and the
                                    // tcgen05 kernel's work queue at byte 64)
 // Work items of the tcgen05 kernel: chunks of at most this many keys.
-constexpr int kTcChunk = 1024;
+constexpr int kTcChunk = 2048;
 
 struct Plan {
     bool mma;

@@ -18,6 +18,9 @@ tc_merge_kernel(const DecodeParams p) {
     const int unit = blockIdx.x / (kTcRows / kTcMergeRows), b = unit / p.Hkv, hk = unit - b * p.Hkv;
     const int r = (blockIdx.x % (kTcRows / kTcMergeRows)) * kTcMergeRows + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (r >= p.M) return;
+    // launched as a programmatic dependent of the main kernel: wait for it to
+    // complete (and its partials to be visible) before reading them
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int L = clamp_len(p, b, false), vis = L - visible_lo(p, L);
     const int nch = (vis + p.chunk - 1) / p.chunk;
     if (nch <= 1) return;
@@ -74,10 +77,20 @@ static cudaError_t launch_tc(const CUtensorMap& kvmap, const CUtensorMap& qmap, 
     kern<<<grid, kTcThreads, TcShape::SMEM, stream>>>(kvmap, qmap, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    // the chunk partials of split units, merged by LSE
+    // the chunk partials of split units, merged by LSE; a programmatic
+    // dependent launch, so that its CTAs are resident when the main kernel ends
     if (p.max_splits > 1) {
-        tc_merge_kernel<<<p.B * p.Hkv * (kTcRows / kTcMergeRows), kTcMergeRows * 32, 0, stream>>>(p);
-        e = cudaGetLastError();
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(p.B * p.Hkv * (kTcRows / kTcMergeRows));
+        cfg.blockDim = dim3(kTcMergeRows * 32);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, tc_merge_kernel, p);
     }
     return e;
 }

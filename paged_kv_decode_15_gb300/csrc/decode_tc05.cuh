@@ -23,8 +23,9 @@
 // Warp roles: warps 0-3 run the softmax, warps 4-7 the epilogue (read O^T,
 // normalise, write out and LSE -- or, for a request split into several
 // chunks, write the chunk's partial result), warp 8 loads (the item's
-// block-table entries, q per item, the K/V tiles), warp 9 issues the MMAs
-// (one thread).  The partials of split requests are merged by LSE in a
+// block-table entries, q per item, the K/V tiles), warp 9 issues S^T = K Q^T
+// and warp 10 O^T += V^T P^T (one thread each, so that a tile's K/V slot is
+// released as soon as its P is written).  The partials of split requests are merged by LSE in a
 // second, short kernel (decode_tc05.cu) launched right after on the same
 // stream: merging inside the persistent kernel left its epilogue warps
 // waiting on chains of L2 round trips at full HBM load.
@@ -45,7 +46,7 @@ constexpr int kTcMaxChunk = 2048; // keys per work item at most
 constexpr int kTcItemPages = kTcMaxChunk / kStageTok + 8;
 constexpr int kTcMaxBatch = 512;  // requests whose lengths and item counts the CTA keeps in shared memory
 constexpr int kTcPageRegs = (kTcItemPages + 31) / 32;  // block-table entries of an item per producer lane
-constexpr int kTcThreads = 320;   // softmax, epilogue (four warps each), loads, MMAs
+constexpr int kTcThreads = 352;   // softmax, epilogue (four warps each), loads, S MMAs, O MMAs
 constexpr float kTcRescale = 8.f; // log2 units: P stays below 2^8 between rescales
 
 struct TcItem {
@@ -74,7 +75,7 @@ struct TcShape {
     static constexpr int B_TF = 0, B_TE = B_TF + kTcNS, B_QF = B_TE + kTcNS, B_QE = B_QF + 2;
     static constexpr int B_SF = B_QE + 2, B_SE = B_SF + 2, B_PF = B_SE + 2, B_PD = B_PF + 1;
     static constexpr int B_OF = B_PD + 1, B_OE = B_OF + 2, B_XF = B_OE + 2, B_XE = B_XF + 2;
-    static constexpr int B_IF = B_XE + 2, B_IE = B_IF + kTcNI, B_DR = B_IE + kTcNI, NBAR = B_DR + 1;
+    static constexpr int B_IF = B_XE + 2, B_IE = B_IF + kTcNI, B_DR = B_IE + kTcNI, NBAR = B_DR + 2;
     static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_TMEM + 16 + 1024;
     static_assert(SMEM <= 227 * 1024, "shared memory of one CTA");
@@ -183,9 +184,10 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
         mbar_init(bar(S::B_PD), 1);
         for (int i = 0; i < kTcNI; ++i) {
             mbar_init(bar(S::B_IF + i), 32);
-            mbar_init(bar(S::B_IE + i), 1 + 128 + 128);  // the MMA thread, softmax and epilogue groups
+            mbar_init(bar(S::B_IE + i), 2 + 128 + 128);  // both MMA threads, softmax and epilogue groups
         }
         mbar_init(bar(S::B_DR), 1);
+        mbar_init(bar(S::B_DR + 1), 1);
         fence_barrier_init();
     }
     if (warp == 9) {
@@ -238,6 +240,9 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
     tc05::fence_before_sync();
     __syncthreads();
     tc05::fence_after_sync();
+    // the merge kernel may be scheduled from now on; it waits for this grid to
+    // complete before it reads anything this grid writes
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const uint32_t tmem = *tslot;
     const int n_items = pref[p.B];
     constexpr uint32_t kIdS = tc05::idesc_f16(kBF16, kTcTile, kTcRows, false, false);  // S^T = K Q^T
@@ -366,26 +371,10 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
             for (int j = max(0, qiss - 2); j < qiss; ++j) mbar_wait(bar(S::B_QF + (j & 1)), (j >> 1) & 1);
         }
     } else if (warp == 9) {
-        // ----------------------------------------------------------- MMAs
+        // ----------------------------------------------------- S^T = K Q^T
         if (lane == 0) {
-            bool ok = true, have = false;
-            int t = 0, pt = 0, pit = 0, pfirst = 0, plast = 0;  // the tile whose O^T += V^T P^T is pending
-            auto issue_pv = [&]() -> bool {
-                const int ts = pt % kTcNS, ob = pit & 1;
-                if (!mbar_wait(bar(S::B_PF), pt & 1, p.status)) return false;
-                if (pfirst && pit >= 2 && !mbar_wait(bar(S::B_OE + ob), ((pit >> 1) - 1) & 1, p.status)) return false;
-                tc05::fence_after_sync();
-                const uint32_t tile = sb0 + S::OFF_KV + ts * S::TILE, ptile = sb0 + S::OFF_P;
-#pragma unroll
-                for (int j = 0; j < kTcTile / 16; ++j)
-                    tc05::mma_f16(tmem + 64 + 32 * ob, tc05::smem_desc(tile + 2 * j * S::GROUP + 2048, 1024, S::GROUP),
-                                  tc05::smem_desc(ptile + (j >> 2) * 4096 + (j & 3) * 32, 16, 1024), kIdO,
-                                  !(pfirst && j == 0));
-                tc05::commit(bar(S::B_PD));
-                tc05::commit(bar(S::B_TE + ts));
-                if (plast) tc05::commit(bar(S::B_OF + ob));
-                return true;
-            };
+            bool ok = true;
+            int t = 0;
             for (int it = 0; ok; ++it) {
                 const int slot = it % kTcNI;
                 if (!mbar_wait(bar(S::B_IF + slot), (it / kTcNI) & 1, p.status)) { ok = false; break; }
@@ -407,19 +396,48 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
                                       tc05::smem_desc(qt + (kk >> 2) * 4096 + (kk & 3) * 32, 16, 1024), kIdS, kk > 0);
                     tc05::commit(bar(S::B_SF + sbuf));
                     if (k == ntiles - 1) tc05::commit(bar(S::B_QE + qb));
-                    if (have && !issue_pv()) { ok = false; break; }
-                    pt = t;
-                    pit = it;
-                    pfirst = k == 0;
-                    plast = k == ntiles - 1;
-                    have = true;
                 }
             }
-            if (ok && have) ok = issue_pv();
             if (!ok) raise_status(p, kErrTimeout);
             // every product issued has completed before TMEM is freed
             tc05::commit(bar(S::B_DR));
             mbar_wait(bar(S::B_DR), 0);
+        }
+        __syncwarp();
+    } else if (warp == 10) {
+        // ------------------------------------------------- O^T += V^T P^T
+        // issued as soon as the softmax has written P, so that the tile's
+        // K/V slot is released without waiting for the next tile's keys
+        if (lane == 0) {
+            bool ok = true;
+            int t = 0;
+            for (int it = 0; ok; ++it) {
+                const int slot = it % kTcNI, ob = it & 1;
+                if (!mbar_wait(bar(S::B_IF + slot), (it / kTcNI) & 1, p.status)) { ok = false; break; }
+                const TcItem& I = items[slot];
+                if (I.end) break;
+                const int ntiles = I.ntiles;
+                mbar_arrive(bar(S::B_IE + slot));
+                for (int k = 0; k < ntiles; ++k, ++t) {
+                    const int ts = t % kTcNS;
+                    if (!mbar_wait(bar(S::B_PF), t & 1, p.status)) { ok = false; break; }
+                    if (k == 0 && it >= 2 && !mbar_wait(bar(S::B_OE + ob), ((it >> 1) - 1) & 1, p.status)) { ok = false; break; }
+                    tc05::fence_after_sync();
+                    const uint32_t tile = sb0 + S::OFF_KV + ts * S::TILE, ptile = sb0 + S::OFF_P;
+#pragma unroll
+                    for (int j = 0; j < kTcTile / 16; ++j)
+                        tc05::mma_f16(tmem + 64 + 32 * ob,
+                                      tc05::smem_desc(tile + 2 * j * S::GROUP + 2048, 1024, S::GROUP),
+                                      tc05::smem_desc(ptile + (j >> 2) * 4096 + (j & 3) * 32, 16, 1024), kIdO,
+                                      !(k == 0 && j == 0));
+                    tc05::commit(bar(S::B_PD));
+                    tc05::commit(bar(S::B_TE + ts));
+                    if (k == ntiles - 1) tc05::commit(bar(S::B_OF + ob));
+                }
+            }
+            if (!ok) raise_status(p, kErrTimeout);
+            tc05::commit(bar(S::B_DR + 1));
+            mbar_wait(bar(S::B_DR + 1), 0);
         }
         __syncwarp();
     } else if (warp < 4) {
