@@ -145,7 +145,8 @@ pkd_status pkd_workspace_check(void* workspace, size_t workspace_bytes, void* st
  * keys).  16-bit query blocks of M = sq * num_heads / num_kv_heads = 17-32
  * rows with head_dim 128, no causal mask and batch <= 512 run instead on a
  * persistent kernel with one CTA per SM on the tcgen05 tensor cores: work
- * items of at most chunk_tokens keys (0: 2048, also the maximum), equal within a
+ * items of at most chunk_tokens keys (0: a quarter of the longest visible
+ * range, between 1024 and 2048 keys; 2048 at most), equal within a
  * request, taken from a queue in the workspace; the chunk partials of split
  * requests are merged by a second, short kernel on the same stream (so such
  * calls launch two kernels).  Other 16-bit blocks of 17-32 rows run the

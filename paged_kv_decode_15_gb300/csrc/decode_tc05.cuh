@@ -20,11 +20,12 @@
 // group holding the four 128-byte chunks of its rows (K dims 0-63, K 64-127,
 // V 0-63, V 64-127; 1 KB each, 128-byte swizzle): both products then see
 // rows at a uniform 4 KB stride, and a 16-key stage takes two copies.
-// Warp roles: warps 0-3 run the softmax, warps 4-7 the epilogue (read O^T,
+// Warp roles: warps 0-7 run the softmax in two groups of four, each group
+// taking 16 of the 32 query rows, warps 8-11 the epilogue (read O^T,
 // normalise, write out and LSE -- or, for a request split into several
-// chunks, write the chunk's partial result), warp 8 loads (the item's
-// block-table entries, q per item, the K/V tiles), warp 9 issues S^T = K Q^T
-// and warp 10 O^T += V^T P^T (one thread each, so that a tile's K/V slot is
+// chunks, write the chunk's partial result), warp 12 loads (the item's
+// block-table entries, q per item, the K/V tiles), warp 13 issues S^T = K Q^T
+// and warp 14 O^T += V^T P^T (one thread each, so that a tile's K/V slot is
 // released as soon as its P is written).  The partials of split requests are merged by LSE in a
 // second, short kernel (decode_tc05.cu) launched right after on the same
 // stream: merging inside the persistent kernel left its epilogue warps
@@ -46,7 +47,8 @@ constexpr int kTcMaxChunk = 2048; // keys per work item at most
 constexpr int kTcItemPages = kTcMaxChunk / kStageTok + 8;
 constexpr int kTcMaxBatch = 512;  // requests whose lengths and item counts the CTA keeps in shared memory
 constexpr int kTcPageRegs = (kTcItemPages + 31) / 32;  // block-table entries of an item per producer lane
-constexpr int kTcThreads = 352;   // softmax, epilogue (four warps each), loads, S MMAs, O MMAs
+constexpr int kTcThreads = 480;   // two softmax groups and the epilogue (four warps each), loads, S MMAs, O MMAs
+constexpr int kTcGroupRows = 16;  // query rows of a softmax group
 constexpr float kTcRescale = 8.f; // log2 units: P stays below 2^8 between rescales
 
 struct TcItem {
@@ -116,6 +118,32 @@ __device__ __forceinline__ float tc_row_reduce(const float (&v)[32], int lane, O
     return op(up ? d[1] : d[0], __shfl_xor_sync(kFull, up ? d[0] : d[1], 1));
 }
 
+// The same for 16 rows: lanes 2r and 2r + 1 both return the reduction of row r.
+template <class Op>
+__device__ __forceinline__ float tc_row_reduce16(const float (&v)[16], int lane, Op op) {
+    float b[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const bool up = lane & 16;
+        b[i] = op(up ? v[i + 8] : v[i], __shfl_xor_sync(kFull, up ? v[i] : v[i + 8], 16));
+    }
+    float c[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const bool up = lane & 8;
+        c[i] = op(up ? b[i + 4] : b[i], __shfl_xor_sync(kFull, up ? b[i] : b[i + 4], 8));
+    }
+    float d[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const bool up = lane & 4;
+        d[i] = op(up ? c[i + 2] : c[i], __shfl_xor_sync(kFull, up ? c[i] : c[i + 2], 4));
+    }
+    const bool up = lane & 2;
+    const float e = op(up ? d[1] : d[0], __shfl_xor_sync(kFull, up ? d[0] : d[1], 2));
+    return op(e, __shfl_xor_sync(kFull, e, 1));
+}
+
 // A four-warp group's own barrier: named barrier `id`, 128 threads.
 __device__ __forceinline__ void tc_group_sync(int id) { asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory"); }
 
@@ -134,6 +162,13 @@ __device__ __forceinline__ int tc_vote(int* votes, int id, int& nvote, int q4, i
 // A wait every lane of the warp takes, with a warp-uniform result.
 __device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity, const DecodeParams& p, uint64_t limit) {
     return __all_sync(kFull, mbar_wait(bar, parity, p.status, limit));
+}
+
+__device__ __forceinline__ float tc_pick16(const float (&v)[16], int r) {
+    float x = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) x = i == r ? v[i] : x;
+    return x;
 }
 
 // Element r of a register array, r not known at compile time (no local memory).
@@ -174,27 +209,27 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
             mbar_init(bar(S::B_QF + i), 1);
             mbar_init(bar(S::B_QE + i), 1);
             mbar_init(bar(S::B_SF + i), 1);
-            mbar_init(bar(S::B_SE + i), 128);
+            mbar_init(bar(S::B_SE + i), 256);
             mbar_init(bar(S::B_OF + i), 1);
             mbar_init(bar(S::B_OE + i), 128);
-            mbar_init(bar(S::B_XF + i), 128);
+            mbar_init(bar(S::B_XF + i), 256);
             mbar_init(bar(S::B_XE + i), 128);
         }
-        mbar_init(bar(S::B_PF), 128);
+        mbar_init(bar(S::B_PF), 256);
         mbar_init(bar(S::B_PD), 1);
         for (int i = 0; i < kTcNI; ++i) {
             mbar_init(bar(S::B_IF + i), 32);
-            mbar_init(bar(S::B_IE + i), 2 + 128 + 128);  // both MMA threads, softmax and epilogue groups
+            mbar_init(bar(S::B_IE + i), 2 + 256 + 128);  // both MMA threads, softmax and epilogue groups
         }
         mbar_init(bar(S::B_DR), 1);
         mbar_init(bar(S::B_DR + 1), 1);
         fence_barrier_init();
     }
-    if (warp == 9) {
+    if (warp == 13) {
         tc05::alloc(smem_u32(tslot), 128);  // S^T: columns 0-63 (two buffers), O^T: 64-127 (two)
         tc05::relinquish_alloc_permit();
     }
-    if (warp == 8) {
+    if (warp == 12) {
         // work items per request (chunks x kv heads), prefix in pref[0..B]
         int run = 0;
         for (int b0 = 0; b0 < p.B; b0 += 32) {
@@ -223,9 +258,9 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
         }
         fence_proxy_async();
     }
-    if (warp >= 4 && warp < 8) {
+    if (warp >= 8 && warp < 12) {
         // requests without a visible key: out = 0, lse = -inf
-        const int et = tid - 128;
+        const int et = tid - 256;
         for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
             const int L = clamp_len(p, b, false);
             if (L - visible_lo(p, L) > 0) continue;
@@ -248,7 +283,7 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
     constexpr uint32_t kIdS = tc05::idesc_f16(kBF16, kTcTile, kTcRows, false, false);  // S^T = K Q^T
     constexpr uint32_t kIdO = tc05::idesc_f16(kBF16, kTcTile, kTcRows, true, false);   // O^T += V^T P^T
 
-    if (warp == 8) {
+    if (warp == 12) {
         // ---------------------------------------------------------- loads
         const uint64_t pol = policy_evict_first();
         if (lane == 0) {
@@ -370,7 +405,7 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
             for (int j = max(0, tiss - kTcNS); j < tiss; ++j) mbar_wait(bar(S::B_TF + j % kTcNS), (j / kTcNS) & 1);
             for (int j = max(0, qiss - 2); j < qiss; ++j) mbar_wait(bar(S::B_QF + (j & 1)), (j >> 1) & 1);
         }
-    } else if (warp == 9) {
+    } else if (warp == 13) {
         // ----------------------------------------------------- S^T = K Q^T
         if (lane == 0) {
             bool ok = true;
@@ -404,7 +439,7 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
             mbar_wait(bar(S::B_DR), 0);
         }
         __syncwarp();
-    } else if (warp == 10) {
+    } else if (warp == 14) {
         // ------------------------------------------------- O^T += V^T P^T
         // issued as soon as the softmax has written P, so that the tile's
         // K/V slot is released without waiting for the next tile's keys
@@ -440,26 +475,32 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
             mbar_wait(bar(S::B_DR + 1), 0);
         }
         __syncwarp();
-    } else if (warp < 4) {
+    } else if (warp < 8) {
         // ------------------------------------------------------- softmax
-        const int q4 = warp, key = 32 * q4 + lane;   // TMEM lane of S^T
+        // two groups of four warps: group g takes query rows 16g .. 16g+15
+        // (columns of S^T and O^T), with votes and reductions of its own
+        constexpr int RG = kTcGroupRows;
+        const int grp = warp >> 2, q4 = warp & 3, rbase = RG * grp, key = 32 * q4 + lane;  // key: TMEM lane of S^T
+        const int gid = 1 + 2 * grp;  // the group's named barrier
+        int* gvotes = votes + 8 * grp;
+        float* gred = red + grp * 2 * RG * 4;
         const uint32_t lane_addr = static_cast<uint32_t>(32 * q4) << 16;
         const float scale2 = p.scale_log2;
         int nvote = 0, t = 0;
-        float m_used[32], lp[32];
+        float m_used[RG], lp[RG];
         for (int it = 0;; ++it) {
             const int slot = it % kTcNI, ob = it & 1;
             const int fail = !tc_wait(bar(S::B_IF + slot), (it / kTcNI) & 1, p, kWaitNs);
             const TcItem& I = items[slot];
             const int end = fail ? 1 : I.end;
-            if (tc_vote(votes, 1, nvote, q4, lane, (fail ? 2 : 0) | (end ? 1 : 0))) {
+            if (tc_vote(gvotes, gid, nvote, q4, lane, (fail ? 2 : 0) | (end ? 1 : 0))) {
                 if (fail) raise_status(p, kErrTimeout);
                 break;
             }
             const int t0 = I.t0, t1 = I.t1, ntiles = I.ntiles, bad = I.bad;
             const int col0 = page_div(t0, p.pmagic, p.pmshift);
 #pragma unroll
-            for (int r = 0; r < 32; ++r) {
+            for (int r = 0; r < RG; ++r) {
                 m_used[r] = -INFINITY;
                 lp[r] = 0.f;
             }
@@ -470,25 +511,26 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
                 const int nvalid = min(kTcTile, t1 - tok0);
                 bool valid = key < nvalid;
                 if (bad && valid) valid = I.pages[page_div(tok0 + key, p.pmagic, p.pmshift) - col0] >= 0;
-                float x[32];
+                float x[RG];
                 const bool got = tc_wait(bar(S::B_SF + sbuf), (t >> 1) & 1, p, kWaitNs);
                 if (got) {
                     tc05::fence_after_sync();
-                    uint32_t sr[32];
-                    tc05::ld_32x32b_x32(tmem + lane_addr + 32 * sbuf, sr);
+                    uint32_t sr[RG];
+                    tc05::ld_32x32b_x16(tmem + lane_addr + 32 * sbuf + rbase, sr);
                     tc05::wait_ld();
                     tc05::fence_before_sync();
                     mbar_arrive(bar(S::B_SE + sbuf));
 #pragma unroll
-                    for (int r = 0; r < 32; ++r) x[r] = (valid && r < M) ? __uint_as_float(sr[r]) * scale2 : -INFINITY;
+                    for (int r = 0; r < RG; ++r)
+                        x[r] = (valid && rbase + r < M) ? __uint_as_float(sr[r]) * scale2 : -INFINITY;
                 } else {
 #pragma unroll
-                    for (int r = 0; r < 32; ++r) x[r] = -INFINITY;
+                    for (int r = 0; r < RG; ++r) x[r] = -INFINITY;
                 }
                 int need = 0;
 #pragma unroll
-                for (int r = 0; r < 32; ++r) need |= x[r] > m_used[r] + kTcRescale;
-                const int v = tc_vote(votes, 1, nvote, q4, lane, (got ? 0 : 2) | need);
+                for (int r = 0; r < RG; ++r) need |= x[r] > m_used[r] + kTcRescale;
+                const int v = tc_vote(gvotes, gid, nvote, q4, lane, (got ? 0 : 2) | need);
                 if (v & 2) {
                     raise_status(p, kErrTimeout);
                     abort = true;
@@ -496,20 +538,20 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
                 }
                 if (v & 1) {
                     // a row's maximum grew past the reference: new references from
-                    // the tile's row maxima, and O and l rescaled to them
-                    // lane r works out row r's new reference and factor, then
-                    // every lane takes them by shuffle
-                    float* rb = red + (nvote & 1) * kTcRows * 4;
-                    const float y = tc_row_reduce(x, lane, [](float a, float b2) { return fmaxf(a, b2); });
-                    rb[lane * 4 + q4] = y;
-                    tc_group_sync(1);
-                    const float4 w = *reinterpret_cast<const float4*>(rb + lane * 4);
-                    const float m_old = tc_pick(m_used, lane);
+                    // the tile's row maxima (lanes 2r and 2r+1 reduce row r), and O
+                    // and l rescaled to them
+                    float* rb = gred + (nvote & 1) * RG * 4;
+                    const float y = tc_row_reduce16(x, lane, [](float a, float b2) { return fmaxf(a, b2); });
+                    if ((lane & 1) == 0) rb[(lane >> 1) * 4 + q4] = y;
+                    tc_group_sync(gid);
+                    const int rl = lane & (RG - 1);
+                    const float4 w = *reinterpret_cast<const float4*>(rb + rl * 4);
+                    const float m_old = tc_pick16(m_used, rl);
                     const float m_new = fmaxf(m_old, fmaxf(fmaxf(w.x, w.y), fmaxf(w.z, w.w)));
                     const float a_lane = m_new == m_old ? 1.f : fast_exp2(m_old - m_new);
                     const bool grew = __any_sync(kFull, m_new > m_old);
 #pragma unroll
-                    for (int r = 0; r < 32; ++r) {
+                    for (int r = 0; r < RG; ++r) {
                         m_used[r] = __shfl_sync(kFull, m_new, r);
                         lp[r] *= __shfl_sync(kFull, a_lane, r);
                     }
@@ -517,13 +559,13 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
                         // O holds the item's earlier tiles: rescale once their P.V has completed
                         if (tc_wait(bar(S::B_PD), (t - 1) & 1, p, kWaitNs)) {
                             tc05::fence_after_sync();
-                            uint32_t o[32];
-                            tc05::ld_32x32b_x32(tmem + lane_addr + 64 + 32 * ob, o);
+                            uint32_t o[RG];
+                            tc05::ld_32x32b_x16(tmem + lane_addr + 64 + 32 * ob + rbase, o);
                             tc05::wait_ld();
 #pragma unroll
-                            for (int r = 0; r < 32; ++r)
+                            for (int r = 0; r < RG; ++r)
                                 o[r] = __float_as_uint(__uint_as_float(o[r]) * __shfl_sync(kFull, a_lane, r));
-                            tc05::st_32x32b_x32(tmem + lane_addr + 64 + 32 * ob, o);
+                            tc05::st_32x32b_x16(tmem + lane_addr + 64 + 32 * ob + rbase, o);
                             tc05::wait_st();
                         } else {
                             abort = true;  // reported at the next vote
@@ -532,9 +574,9 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
                 }
                 // P (rows past M and keys outside the chunk are 0), once the previous
                 // tile's P.V has read the buffer
-                float pr[32];
+                float pr[RG];
 #pragma unroll
-                for (int r = 0; r < 32; ++r) {
+                for (int r = 0; r < RG; ++r) {
                     pr[r] = m_used[r] == -INFINITY ? 0.f : fast_exp2(x[r] - m_used[r]);
                     lp[r] += pr[r];
                 }
@@ -542,21 +584,24 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
                 uint8_t* ptile = smem + S::OFF_P + (key >> 6) * 4096;
                 const int kc = (key & 63) >> 3, kb2 = (key & 7) * 2;
 #pragma unroll
-                for (int r = 0; r < 32; ++r) {
+                for (int r = 0; r < RG; ++r) {
+                    const int row = rbase + r;
                     const uint32_t h = pack2<kBF16>(pr[r], 0.f);
-                    *reinterpret_cast<uint16_t*>(ptile + r * 128 + (((kc ^ (r & 7)) << 4) | kb2)) =
+                    *reinterpret_cast<uint16_t*>(ptile + row * 128 + (((kc ^ (row & 7)) << 4) | kb2)) =
                         static_cast<uint16_t>(h & 0xffffu);
                 }
-                if (__any_sync(kFull, !valid)) {
+                if (grp == 0 && __any_sync(kFull, !valid)) {
                     // keys outside the chunk (or on a skipped page) get P = 0; their V
-                    // rows, stale or never loaded, are zeroed so that 0 * NaN cannot occur
+                    // rows, stale or never loaded, are zeroed so that 0 * NaN cannot
+                    // occur (each lane starts at its own chunk: no bank conflicts)
                     if (!tc_wait(bar(S::B_TF + ts), (t / kTcNS) & 1, p, kWaitNs)) abort = true;
                     if (!valid) {
                         uint8_t* vrow = smem + S::OFF_KV + ts * S::TILE + (key >> 3) * S::GROUP + 2048 + (key & 7) * 128;
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
-                            *reinterpret_cast<uint4*>(vrow + j * 16) = make_uint4(0, 0, 0, 0);
-                            *reinterpret_cast<uint4*>(vrow + 1024 + j * 16) = make_uint4(0, 0, 0, 0);
+                            const int c = ((j + lane) & 7) * 16;
+                            *reinterpret_cast<uint4*>(vrow + c) = make_uint4(0, 0, 0, 0);
+                            *reinterpret_cast<uint4*>(vrow + 1024 + c) = make_uint4(0, 0, 0, 0);
                         }
                     }
                 }
@@ -564,16 +609,16 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
                 tc05::fence_before_sync();
                 mbar_arrive(bar(S::B_PF));
             }
-            if (tc_vote(votes, 1, nvote, q4, lane, abort ? 2 : 0) & 2) {
+            if (tc_vote(gvotes, gid, nvote, q4, lane, abort ? 2 : 0) & 2) {
                 raise_status(p, kErrTimeout);
                 break;
             }
             // row statistics for the epilogue: this warp's share of l, and m
-            const float lw = tc_row_reduce(lp, lane, [](float a, float b2) { return a + b2; });
+            const float lw = tc_row_reduce16(lp, lane, [](float a, float b2) { return a + b2; });
             const bool free_ok = it < 2 || tc_wait(bar(S::B_XE + ob), ((it >> 1) - 1) & 1, p, kWaitNs);
             float* st = stats + ob * 5 * kTcRows;
-            st[q4 * kTcRows + lane] = lw;
-            if (q4 == 0) st[4 * kTcRows + lane] = tc_pick(m_used, lane);
+            if ((lane & 1) == 0) st[q4 * kTcRows + rbase + (lane >> 1)] = lw;
+            if (q4 == 0 && lane < RG) st[4 * kTcRows + rbase + lane] = tc_pick16(m_used, lane);
             mbar_arrive(bar(S::B_XF + ob));
             mbar_arrive(bar(S::B_IE + slot));
             if (!free_ok) {
@@ -582,9 +627,9 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
         }
     } else {
         // ------------------------------------------------------ epilogue
-        const int q4 = warp - 4, et = tid - 128, d = 32 * q4 + lane;  // TMEM lane of O^T: the head dim
+        const int q4 = warp & 3, et = tid - 256, d = 32 * q4 + lane;  // TMEM lane of O^T: the head dim
         const uint32_t lane_addr = static_cast<uint32_t>(32 * q4) << 16;
-        int* evotes = votes + 8;
+        int* evotes = votes + 16;
         int nvote = 0;
         for (int it = 0;; ++it) {
             const int slot = it % kTcNI, ob = it & 1;
@@ -655,7 +700,7 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
     // ---------------------------------------------------------- tear-down
     tc05::fence_before_sync();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == 13) {
         tc05::fence_after_sync();
         tc05::dealloc(tmem, 128);
     }
