@@ -83,29 +83,35 @@ def load_peaks() -> dict:
 
 # sources that build neither the paged-decode kernels nor their launch plan
 NON_DECODE_SOURCES = ("segment.cu", "segment.cuh", "cache_write.cu", "static_ws.cu")
+# sources of the tcgen05 query-block kernel only
+TC05_SOURCES = ("decode_tc05.cu", "decode_tc05.cuh", "tc05.cuh")
 
 
-def source_digest() -> str:
-    """sha256 over the paged-decode kernel sources and their launch plan: a
-    traffic figure is valid only for this digest."""
+def source_digest(tc05: bool = True) -> str:
+    """sha256 over the paged-decode kernel sources and their launch plan (with
+    tc05=False, leaving out the files only the tcgen05 kernel is built from):
+    a traffic figure is valid only for the digest of the sources its kernel
+    is built from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_decode_15_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")) and name not in NON_DECODE_SOURCES:
+        if name.endswith((".cu", ".cuh", ".h")) and name not in NON_DECODE_SOURCES and \
+                (tc05 or name not in TC05_SOURCES):
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
-    """dram bytes per launch from the committed ncu summary, if it matches these sources."""
+def profiled_traffic(workload: str, kernel: str = ""):
+    """dram bytes per launch from the committed ncu summary, if it matches the
+    sources of the kernel the workload runs (`kernel`: the library's name)."""
     path = os.path.join(ROOT, "profiles", f"decode_{workload}.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
     t = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
     d = re.search(r"source_digest:\s*([0-9a-f]+)", text)
-    if not t or not d or d.group(1) != source_digest():
+    if not t or not d or d.group(1) != source_digest(tc05="tcgen05" in kernel):
         return None
     return int(t.group(1))
 
@@ -669,7 +675,7 @@ def main():
         gbs = job_throughput(acct["kv"], world, steps, total_ms)
         avg_ms = total_ms / steps
         achieved = acct["total"] / (avg_ms / 1e3) / 1e9
-        traffic = profiled_traffic(case.name)
+        traffic = profiled_traffic(case.name, paged_kernel_name(case, args) if kind_is_paged else "")
         line = {
             "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world, "steps": steps,
             "warmup": args.warmup, "ms_per_step": round(avg_ms, 5), "higher_is_better": True, "scaling": "weak",
