@@ -144,12 +144,14 @@ pkd_status pkd_workspace_check(void* workspace, size_t workspace_bytes, void* st
  * most 4096 keys -- 32 chunks for 64 (request, kv head) units of 131,072
  * keys).  16-bit query blocks of M = sq * num_heads / num_kv_heads = 17-32
  * rows with head_dim 128, no causal mask and batch <= 512 run instead on a
- * persistent kernel with one CTA per SM on the tcgen05 tensor cores: work
- * items of at most chunk_tokens keys (0: a quarter of the longest visible
- * range, between 1024 and 2048 keys; 2048 at most), equal within a
- * request, taken from a queue in the workspace; the chunk partials of split
- * requests are merged by a second, short kernel on the same stream (so such
- * calls launch two kernels).  Other 16-bit blocks of 17-32 rows run the
+ * persistent kernel with one CTA per SM on the tcgen05 tensor cores: chunks
+ * of at most chunk_tokens keys (0: a quarter of the longest visible range in
+ * whole 128-key tiles, between 1024 and 2048 keys; 2048 at most), equal
+ * within a request; with more chunks than SMs every CTA takes an equal
+ * share of all 128-key tiles (consecutive chunks of a (request, kv head)
+ * accumulate together), and only units cut by a share boundary leave
+ * partial results, merged by LSE by the CTA that completes the unit's last
+ * piece -- one launch.  Other 16-bit blocks of 17-32 rows run the
  * chunked grid with two warps sharing each chunk's stages, 16 rows each
  * (as few chunks of at most 4096 keys as possible).  fp8
  * caches with M > 16 run, for batch <= 1024, on a persistent grid that gives

@@ -46,9 +46,8 @@ int elt_bytes(pkd_dtype dt) { return dt == PKD_FP8_E4M3 ? 1 : dt == PKD_FP32 ? 4
 // gqa_decode_b64 (M = 4) 2048 (1024-key chunks) beats 512- to 2048-key chunks.
 constexpr int kTargetCtas = 2048;
 constexpr int kMaxChunk = 4096;    // and never puts more keys than this in one chunk
-constexpr size_t kHeader = 256;    // workspace status word lives in the first bytes (and the
-                                   // tcgen05 kernel's work queue at byte 64)
-// Work items of the tcgen05 kernel: automatic chunks of at least this many keys.
+constexpr size_t kHeader = 256;    // workspace status word lives in the first bytes
+// Chunks of the tcgen05 kernel: automatic chunks of at least this many keys.
 constexpr int kTcChunkMin = 1024;
 
 struct Plan {
@@ -129,19 +128,20 @@ pkd_status make_plan(int B, int sq, int Hq, int Hkv, int D, int P, int max_kv_le
     pl.max_vis = (int)(span < max_kv_len ? span : max_kv_len);
     const int units = B * Hkv > 0 ? B * Hkv : 1;
     if (pl.tc) {
-        // work items of at most `chunk` keys (equal chunks within a request);
-        // each split unit keeps one partial slot of 32 rows per chunk
+        // chunks of at most `chunk` keys (equal within a request, whole 128-key
+        // tiles where the chunk allows); a (request, kv head) unit of n chunks
+        // is one piece per chunk (one chunk per CTA) or per CTA share it meets
+        // (shares at least a chunk long): at most n + 1 partial slots of 32
+        // rows, and an arrival counter
         if (chunk_tokens > 0 && chunk_tokens % P != 0)
             return fail(PKD_EINVAL, "chunk_tokens %d must be a multiple of page_size %d", chunk_tokens, P);
-        // automatic: a quarter of the longest visible range, 1024-2048 keys, a
-        // multiple of the page (query_block_sq8, 8192 keys: 2048, 128.5 us against
-        // 129.8 with 1024; with window 4096, 4111 keys: 1040, 106.6 us against 111.2
-        // with 2048)
-        int auto_chunk = (pl.max_vis / 4 + P - 1) / P * P;
-        if (auto_chunk < kTcChunkMin) auto_chunk = (kTcChunkMin + P - 1) / P * P;
-        if (auto_chunk > pkd::kTcMaxChunk) auto_chunk = pkd::kTcMaxChunk / P * P;
+        // automatic: a quarter of the longest visible range in whole tiles,
+        // 1024-2048 keys
+        int auto_chunk = (pl.max_vis / 4 + pkd::kTcTile - 1) / pkd::kTcTile * pkd::kTcTile;
+        if (auto_chunk < kTcChunkMin) auto_chunk = kTcChunkMin;
+        if (auto_chunk > pkd::kTcMaxChunk) auto_chunk = pkd::kTcMaxChunk;
         pl.chunk = chunk_tokens > 0 ? chunk_tokens : auto_chunk;
-        pl.max_splits = pl.max_vis > 0 ? (pl.max_vis + pl.chunk - 1) / pl.chunk : 1;
+        pl.max_splits = (pl.max_vis > 0 ? (pl.max_vis + pl.chunk - 1) / pl.chunk : 1) + 1;
         const size_t parts = (size_t)units * pl.max_splits;
         pl.off_counters = kHeader;
         pl.off_lse = pl.off_counters + round_up((size_t)units * 4, 256);
@@ -275,8 +275,9 @@ pkd_status get_map(CUtensorMap& out, const void* base, int rank, uint64_t d0, ui
 // half_rows the box is {one chunk, 8 rows, one chunk}: one copy per chunk
 // fills the first 8 rows of that chunk's 16-row slot.
 // Boxes of the stage map: a whole 16-key stage (every chunk), its first 8
-// rows of one chunk, or 8 rows of every chunk (a 4 KB group of K and V).
-enum StageBox { kStageFull = 0, kStageHalfRows = 1, kStageGroup8 = 2 };
+// rows of one chunk, or the tcgen05 kernel's group: 8 rows of
+// kTcBoxChunks chunks.
+enum StageBox { kStageFull = 0, kStageHalfRows = 1, kStageTcGroup = 2 };
 
 pkd_status get_stage_map(CUtensorMap& out, const void* cache, uint64_t rows, int row_bytes, pkd_dtype dt,
                          StageBox mode = kStageFull) {
@@ -284,7 +285,7 @@ pkd_status get_stage_map(CUtensorMap& out, const void* cache, uint64_t rows, int
     MapKey k;
     std::memset(&k, 0, sizeof k);
     k.base = cache; k.d0 = 128 / elt; k.d1 = rows; k.d2 = row_bytes / 128; k.s1 = row_bytes; k.s2 = 128;
-    k.rank = mode == kStageHalfRows ? 108 : mode == kStageGroup8 ? 120 : 103; k.dtype = dt;
+    k.rank = mode == kStageHalfRows ? 108 : mode == kStageTcGroup ? 120 + pkd::kTcBoxChunks : 103; k.dtype = dt;
     MapCache& c = map_cache();
     {
         std::lock_guard<std::mutex> g(c.mu);
@@ -302,7 +303,7 @@ pkd_status get_stage_map(CUtensorMap& out, const void* cache, uint64_t rows, int
     cuuint64_t dims[3] = {k.d0, k.d1, k.d2};
     cuuint64_t strides[2] = {k.s1, k.s2};
     cuuint32_t box[3] = {(cuuint32_t)(128 / elt), (cuuint32_t)(mode == kStageFull ? pkd::kStageTok : pkd::kStageTok / 2),
-                         (cuuint32_t)(mode == kStageHalfRows ? 1 : row_bytes / 128)};
+                         (cuuint32_t)(mode == kStageHalfRows ? 1 : mode == kStageTcGroup ? pkd::kTcBoxChunks : row_bytes / 128)};
     cuuint32_t estr[3] = {1, 1, 1};
     CUtensorMap m;
     CUresult r = enc(&m, t, 3, const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -494,11 +495,10 @@ pkd_status pkd_paged_decode(const void* q, pkd_dtype q_dtype, const void* kv_cac
     const int max_ctas = pkd::kFlatMaxWorkers / pkd::kNW;
     if (pl.tc) {
         CUtensorMap kvmap, qmap;
-        st = get_stage_map(kvmap, kv_cache, rows, 2 * head_dim * elt, kv_dtype, kStageGroup8);
+        st = get_stage_map(kvmap, kv_cache, rows, 2 * head_dim * elt, kv_dtype, kStageTcGroup);
         if (st != PKD_OK) return st;
         st = get_q_map(qmap, q, head_dim, num_heads, (uint64_t)batch * sq, pl.G, sq, kv_dtype);
         if (st != PKD_OK) return st;
-        p.sched = reinterpret_cast<int32_t*>(ws + 64);
         e = pkd::launch_decode_tc05(kv_dtype == PKD_BF16, kvmap, qmap, p, s);
     } else if (pl.bal)
         e = pkd::launch_decode_bal(head_dim, kv_dtype == PKD_BF16, pl.mt, pl.nt, tmap, p, s);

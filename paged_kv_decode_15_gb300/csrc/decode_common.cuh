@@ -37,7 +37,6 @@ struct DecodeParams {
     float scale_log2;            // scale * q_scale * k_scale * log2(e)
     float v_scale;
     uint64_t wait_ns;            // limit of a wait on a stage's copy (0: test once)
-    int32_t* sched;              // persistent work queue: [0] next item, [32] CTAs done (zeroed)
 };
 
 struct CtaWork {

@@ -1,9 +1,18 @@
 // Paged decode of query blocks with 17-32 rows per kv head (M = sq * Hq/Hkv)
 // on the 5th-generation tensor cores, accumulators in tensor memory (TMEM).
 //
-// One persistent CTA per SM takes work items -- (request, chunk of keys, kv
-// head) -- from a queue in the workspace, so SMs that finish early take more.
-// Per 128-key tile of an item:
+// One persistent CTA per SM.  A request's visible keys are cut into chunks
+// of at most `chunk` keys (whole 128-key tiles where the chunk allows).
+// With no more (request, kv head, chunk) items than CTAs each CTA takes one
+// chunk.  Otherwise the launch's work is the sequence of all tiles in the
+// order (request, kv head, chunk, tile) and each CTA takes an equal share --
+// a contiguous range at least one chunk long -- so that every CTA streams
+// the same number of bytes and none waits for a straggler at the end.  A CTA
+// walks its range as work items of at most one chunk (the block-table entries
+// of an item fit in shared memory); consecutive items of one (request, kv
+// head) unit form a run that keeps accumulating in TMEM, so a unit is split
+// -- partial result per run, merged by LSE -- only where a share boundary
+// cuts it.  Per 128-key tile of an item:
 //   S^T = K Q^T      tcgen05.mma, M = 128 keys, N = 32 query rows, K = 128
 //                    dims: A = the K tile as TMA lands it (K-major, 128-byte
 //                    swizzle), B = the item's q rows (K-major); S^T in TMEM.
@@ -15,21 +24,21 @@
 //                    type.
 //   O^T += V^T P^T   M = 128 dims, N = 32 rows, K = 128 keys: A = the V tile
 //                    read MN-major, B = P (K-major); O^T accumulates in TMEM
-//                    over the item's tiles.
+//                    over the run's tiles.
 // A tile lands as sixteen 4 KB groups of 8 keys, one TMA copy each, every
 // group holding the four 128-byte chunks of its rows (K dims 0-63, K 64-127,
 // V 0-63, V 64-127; 1 KB each, 128-byte swizzle): both products then see
 // rows at a uniform 4 KB stride, and a 16-key stage takes two copies.
 // Warp roles: warps 0-7 run the softmax in two groups of four, each group
 // taking 16 of the 32 query rows, warps 8-11 the epilogue (read O^T,
-// normalise, write out and LSE -- or, for a request split into several
-// chunks, write the chunk's partial result), warp 12 loads (the item's
-// block-table entries, q per item, the K/V tiles), warp 13 issues S^T = K Q^T
-// and warp 14 O^T += V^T P^T (one thread each, so that a tile's K/V slot is
-// released as soon as its P is written).  The partials of split requests are merged by LSE in a
-// second, short kernel (decode_tc05.cu) launched right after on the same
-// stream: merging inside the persistent kernel left its epilogue warps
-// waiting on chains of L2 round trips at full HBM load.
+// normalise, write out and LSE -- or, for a unit split into several runs,
+// write the run's partial result), warp 12 loads (the item's block-table
+// entries, q per run, the K/V tiles), warp 13 issues S^T = K Q^T and warp 14
+// O^T += V^T P^T (one thread each, so that a tile's K/V slot is released as
+// soon as its P is written).  A split unit's runs count their arrivals in
+// the workspace; the epilogue of the CTA that completes the last one merges
+// the partials by LSE (at most a few units per CTA, the shares being at
+// least a chunk long).
 // Every wait is bounded; a failure raises the status word and every role
 // leaves after letting its own copies and products complete.
 #pragma once
@@ -41,20 +50,44 @@ namespace pkd {
 
 constexpr int kTcTile = 128;      // keys per tile: the M of S^T = K Q^T
 constexpr int kTcRows = 32;       // query rows per unit, padded: the N of both products
+constexpr int kTcBoxChunks = 4;  // 128-byte chunks per TMA group copy: K and V
 constexpr int kTcNS = 3;          // K/V tile ring
 constexpr int kTcNI = 4;          // work-item ring
-constexpr int kTcMaxChunk = 2048; // keys per work item at most
+constexpr int kTcMaxChunk = 2048; // keys per chunk at most
 constexpr int kTcItemPages = kTcMaxChunk / kStageTok + 8;
-constexpr int kTcMaxBatch = 512;  // requests whose lengths and item counts the CTA keeps in shared memory
+constexpr int kTcMaxBatch = 512;  // requests whose lengths and work prefix the CTA keeps in shared memory
 constexpr int kTcPageRegs = (kTcItemPages + 31) / 32;  // block-table entries of an item per producer lane
 constexpr int kTcThreads = 480;   // two softmax groups and the epilogue (four warps each), loads, S MMAs, O MMAs
 constexpr int kTcGroupRows = 16;  // query rows of a softmax group
 constexpr float kTcRescale = 8.f; // log2 units: P stays below 2^8 between rescales
 
+// cont: the item continues the previous item's run (same unit, same
+// accumulators); last: the run ends with it (the epilogue follows); slot: the
+// run's partial slot in its unit; pieces: the unit's runs (1: this run is
+// the whole unit).
 struct TcItem {
-    int b, hk, c, nch, t0, t1, ntiles, bad, end, pad[7];
+    int b, hk, slot, pieces, cont, last, t0, t1, ntiles, bad, end, pad[5];
     int pages[kTcItemPages];      // table columns t0/P ..; -1: outside the pool (keys skipped)
 };
+
+// The chunks of a visible range of `vis` keys for chunks of at most C keys:
+// n chunks of `len` keys (whole 128-key tiles unless C is smaller or not a
+// multiple of 128), the last one shorter; all non-empty.
+struct TcChunks {
+    int n, len, tiles_full, tiles_last, tiles;  // tiles: of one kv head, all chunks
+};
+__host__ __device__ __forceinline__ TcChunks tc_chunks(int vis, int C) {
+    TcChunks ch{0, C, 0, 0, 0};
+    if (vis <= 0) return ch;
+    const int n0 = (vis + C - 1) / C, even = (vis + n0 - 1) / n0;
+    const int whole = (even + kTcTile - 1) / kTcTile * kTcTile;
+    ch.len = whole < C ? whole : C;
+    ch.n = (vis + ch.len - 1) / ch.len;
+    ch.tiles_full = (ch.len + kTcTile - 1) / kTcTile;
+    ch.tiles_last = (vis - (ch.n - 1) * ch.len + kTcTile - 1) / kTcTile;
+    ch.tiles = (ch.n - 1) * ch.tiles_full + ch.tiles_last;
+    return ch;
+}
 
 // Shared memory.  Operand regions are 1024-byte aligned (128-byte swizzle atoms).
 struct TcShape {
@@ -68,8 +101,8 @@ struct TcShape {
     static constexpr int OFF_ITEM = OFF_P + PB;
     static constexpr int OFF_STAT = OFF_ITEM + kTcNI * static_cast<int>(sizeof(TcItem));  // [2][4 warps + m][32]
     static constexpr int OFF_RED = OFF_STAT + 2 * 5 * kTcRows * 4;  // float [2][32 rows][4 warps]
-    static constexpr int OFF_VOTE = OFF_RED + 2 * kTcRows * 4 * 4;  // int votes [2][4] per group, merge flag
-    static constexpr int OFF_PREF = OFF_VOTE + 128;                 // int [kTcMaxBatch + 1]
+    static constexpr int OFF_VOTE = OFF_RED + 2 * kTcRows * 4 * 4;  // int votes [2][4] per group; [24]: arrivals
+    static constexpr int OFF_PREF = OFF_VOTE + 128;                 // int [kTcMaxBatch + 1]: work prefix
     static constexpr int OFF_LENS = OFF_PREF + (kTcMaxBatch + 1) * 4;  // int [kTcMaxBatch]: clamped lengths
     static constexpr int OFF_BAR = (OFF_LENS + kTcMaxBatch * 4 + 7) & ~7;
     // barriers: K/V full/empty, q full/empty, S full/empty, P full, P.V done,
@@ -179,6 +212,81 @@ __device__ __forceinline__ float tc_pick(const float (&v)[32], int r) {
     return x;
 }
 
+// LSE merge of the `np` pieces (partial results) of a split unit, run by the
+// epilogue warps of the CTA that completed its last piece.  Warp q4 takes
+// query rows q4, q4 + 4, ... (four at a time); lane j reads piece j's LSE
+// (blocks of 32 pieces) and sums dims 4j .. 4j+3 over the pieces, all loads
+// of a block issued before the first is used.  Pieces were written by other
+// CTAs: L2 loads only.
+__device__ __forceinline__ void tc_merge_unit(const DecodeParams& p, long long unit, long long row0, int np, int q4,
+                                              int lane) {
+    constexpr int R = 4;
+    const float* pl = p.part_lse + unit * p.max_splits * kTcRows;
+    const float* po = p.part_out + unit * p.max_splits * kTcRows * 128 + 4 * lane;
+#pragma unroll 1
+    for (int r0 = q4; r0 < p.M; r0 += 4 * R) {
+        float lc0[R], mx[R], ws[R];
+        float4 acc[R];
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            const int r = r0 + 4 * i;
+            lc0[i] = (lane < np && r < p.M) ? __ldcg(pl + lane * kTcRows + r) : -INFINITY;
+            mx[i] = lc0[i];
+            ws[i] = 0.f;
+            acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        for (int s = 32 + lane; s - lane < np; s += 32)
+#pragma unroll
+            for (int i = 0; i < R; ++i)
+                if (s < np && r0 + 4 * i < p.M) mx[i] = fmaxf(mx[i], __ldcg(pl + s * kTcRows + r0 + 4 * i));
+#pragma unroll
+        for (int i = 0; i < R; ++i)
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mx[i] = fmaxf(mx[i], __shfl_xor_sync(kFull, mx[i], o));
+        for (int s0 = 0; s0 < np; s0 += 32) {
+            const int n = min(32, np - s0);
+            float wl[R];
+#pragma unroll
+            for (int i = 0; i < R; ++i) {
+                const int r = r0 + 4 * i;
+                const float lc = s0 == 0 ? lc0[i]
+                                         : (s0 + lane < np && r < p.M ? __ldcg(pl + (s0 + lane) * kTcRows + r) : -INFINITY);
+                wl[i] = lc == -INFINITY ? 0.f : fast_exp2(lc - mx[i]);
+                ws[i] += wl[i];
+            }
+            for (int j = 0; j < n; ++j) {
+                float4 v[R];
+#pragma unroll
+                for (int i = 0; i < R; ++i)
+                    v[i] = r0 + 4 * i < p.M
+                               ? __ldcg(reinterpret_cast<const float4*>(po + ((s0 + j) * kTcRows + r0 + 4 * i) * 128))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int i = 0; i < R; ++i) {
+                    const float w = __shfl_sync(kFull, wl[i], j);
+                    acc[i] = make_float4(fmaf(w, v[i].x, acc[i].x), fmaf(w, v[i].y, acc[i].y),
+                                         fmaf(w, v[i].z, acc[i].z), fmaf(w, v[i].w, acc[i].w));
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            const int r = r0 + 4 * i;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) ws[i] += __shfl_xor_sync(kFull, ws[i], o);
+            if (r >= p.M) continue;
+            const float sc = ws[i] > 0.f ? p.v_scale / ws[i] : 0.f;
+            const long long orow = row0 + static_cast<long long>(r / p.G) * p.Hq + r % p.G;
+            const long long o0 = orow * 128 + 4 * lane;
+            store_out(p.out, o0 + 0, acc[i].x * sc, p.out_dtype);
+            store_out(p.out, o0 + 1, acc[i].y * sc, p.out_dtype);
+            store_out(p.out, o0 + 2, acc[i].z * sc, p.out_dtype);
+            store_out(p.out, o0 + 3, acc[i].w * sc, p.out_dtype);
+            if (lane == 0 && p.lse) p.lse[orow] = ws[i] > 0.f ? (mx[i] + __log2f(ws[i])) * kLn2 : -INFINITY;
+        }
+    }
+}
+
 template <bool kBF16>
 __global__ void __launch_bounds__(kTcThreads, 1)
 decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_constant__ CUtensorMap qmap,
@@ -229,16 +337,35 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
         tc05::alloc(smem_u32(tslot), 128);  // S^T: columns 0-63 (two buffers), O^T: 64-127 (two)
         tc05::relinquish_alloc_permit();
     }
+    // warp 12: the launch's work -- chunks (item mode, no more than CTAs) or
+    // tiles (share mode) of all requests -- and its prefix per request in pref
+    bool by_item = true;
+    int total = 0;
     if (warp == 12) {
-        // work items per request (chunks x kv heads), prefix in pref[0..B]
+        int n_items = 0, n_tiles = 0;
+        for (int b0 = 0; b0 < p.B; b0 += 32) {
+            const int b = b0 + lane;
+            int ni = 0, nt = 0;
+            if (b < p.B) {
+                const int L = clamp_len(p, b, true);
+                const TcChunks ch = tc_chunks(L - visible_lo(p, L), C);
+                ni = ch.n * Hkv;
+                nt = ch.tiles * Hkv;
+                lens[b] = L;
+            }
+            n_items += __reduce_add_sync(kFull, ni);
+            n_tiles += __reduce_add_sync(kFull, nt);
+        }
+        by_item = n_items <= static_cast<int>(gridDim.x);
+        total = by_item ? n_items : n_tiles;
         int run = 0;
         for (int b0 = 0; b0 < p.B; b0 += 32) {
             const int b = b0 + lane;
             int n = 0;
             if (b < p.B) {
-                const int L = clamp_len(p, b, true), vis = L - visible_lo(p, L);
-                n = vis > 0 ? (vis + C - 1) / C * Hkv : 0;
-                lens[b] = L;
+                const int L = lens[b];
+                const TcChunks ch = tc_chunks(L - visible_lo(p, L), C);
+                n = (by_item ? ch.n : ch.tiles) * Hkv;
             }
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -275,11 +402,7 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
     tc05::fence_before_sync();
     __syncthreads();
     tc05::fence_after_sync();
-    // the merge kernel may be scheduled from now on; it waits for this grid to
-    // complete before it reads anything this grid writes
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const uint32_t tmem = *tslot;
-    const int n_items = pref[p.B];
     constexpr uint32_t kIdS = tc05::idesc_f16(kBF16, kTcTile, kTcRows, false, false);  // S^T = K Q^T
     constexpr uint32_t kIdO = tc05::idesc_f16(kBF16, kTcTile, kTcRows, true, false);   // O^T += V^T P^T
 
@@ -290,54 +413,86 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
             prefetch_tmap(&kvmap);
             prefetch_tmap(&qmap);
         }
-        int t = 0, tiss = 0, qiss = 0, nxt = 0;
+        int t = 0, tiss = 0, qiss = 0;
         bool ok = true;
-        // Work item i: its request, chunk and kv head, and the block-table
-        // entries of its keys, loaded one item ahead into registers (lane j
-        // holds entries j, j + 32, ...) so that they have landed when the item
-        // is published.
+        // This CTA's work, [cur, stop) of the launch's sequence: item
+        // blockIdx.x in item mode; in share mode an equal share of the tiles,
+        // at least one chunk long (so that a unit of n chunks has at most n + 1
+        // pieces).  It is walked item by item, one ahead: the next item is
+        // decoded while this one streams (to know where a run ends), and its
+        // block-table entries are loaded into registers (lane j holds entries
+        // j, j + 32, ...) so that they have landed when it is published.
+        const int G = static_cast<int>(gridDim.x), me = static_cast<int>(blockIdx.x);
+        const int share = max((total + G - 1) / G, (C + kTcTile - 1) / kTcTile);
+        int cur = by_item ? me : static_cast<int>(min(static_cast<long long>(total), static_cast<long long>(me) * share));
+        const int stop = by_item ? min(total, me + 1) : min(total, cur + share);
         struct Work {
-            int i, b, hk, c, nch, t0, t1, ntiles, col0, npg;
+            int b, hk, unit, slot, pieces, t0, t1, ntiles, col0, npg;
+            bool valid, cont;
         };
-        auto decode = [&](int i, Work& x) {
-            x.i = i;
-            if (i >= n_items) return;
-            int lo_b = 0, hi_b = p.B;  // pref[lo_b] <= i < pref[hi_b]
+        int prev_unit = -1;
+        auto next_work = [&](Work& x) {
+            x.valid = cur < stop;
+            if (!x.valid) return;
+            int lo_b = 0, hi_b = p.B;  // pref[lo_b] <= cur < pref[hi_b]
             while (hi_b - lo_b > 1) {
                 const int mid = (lo_b + hi_b) >> 1;
-                if (pref[mid] <= i) lo_b = mid; else hi_b = mid;
+                if (pref[mid] <= cur) lo_b = mid; else hi_b = mid;
             }
-            const int L = lens[lo_b], lo = visible_lo(p, L), vis = L - lo, rem = i - pref[lo_b];
+            const int L = lens[lo_b], lo = visible_lo(p, L);
+            const TcChunks ch = tc_chunks(L - lo, C);
+            const int r = cur - pref[lo_b];
+            int hk, c, k0, k1;
+            if (by_item) {
+                hk = r / ch.n;
+                c = r - hk * ch.n;
+                k0 = 0;
+                k1 = c < ch.n - 1 ? ch.tiles_full : ch.tiles_last;
+                x.slot = c;
+                x.pieces = ch.n;
+            } else {
+                // tile rr of the unit: chunk c, its tile k0
+                hk = r / ch.tiles;
+                const int rr = r - hk * ch.tiles, ustart = cur - rr;
+                c = min(rr / ch.tiles_full, ch.n - 1);
+                k0 = rr - c * ch.tiles_full;
+                k1 = min(c < ch.n - 1 ? ch.tiles_full : ch.tiles_last, k0 + (stop - cur));
+                // the unit's pieces: one per share it meets
+                x.slot = me - ustart / share;
+                x.pieces = (ustart + ch.tiles - 1) / share - ustart / share + 1;
+            }
+            const int cs = lo + c * ch.len, ce = min(cs + ch.len, L);
             x.b = lo_b;
-            x.c = rem / Hkv;
-            x.hk = rem - x.c * Hkv;
-            x.nch = (vis + C - 1) / C;
-            const int cb = ((vis + x.nch - 1) / x.nch + kStageTok - 1) & ~(kStageTok - 1);  // equal chunks, whole stages
-            x.t0 = lo + x.c * cb;
-            x.t1 = min(x.t0 + cb, L);
-            x.ntiles = (x.t1 - x.t0 + kTcTile - 1) / kTcTile;
+            x.hk = hk;
+            x.unit = lo_b * Hkv + hk;
+            x.t0 = cs + k0 * kTcTile;
+            x.t1 = min(cs + k1 * kTcTile, ce);
+            x.ntiles = k1 - k0;
+            x.cont = x.unit == prev_unit;
             x.col0 = page_div(x.t0, p.pmagic, p.pmshift);
             x.npg = page_div(x.t1 - 1, p.pmagic, p.pmshift) - x.col0 + 1;
+            prev_unit = x.unit;
+            cur += by_item ? 1 : k1 - k0;
         };
         int pg_next[kTcPageRegs];
         auto load_pages = [&](const Work& x) {
 #pragma unroll
             for (int k = 0; k < kTcPageRegs; ++k) {
                 const int j = lane + 32 * k;
-                pg_next[k] = (x.i < n_items && j < x.npg)
+                pg_next[k] = (x.valid && j < x.npg)
                                  ? p.block_table[static_cast<long long>(x.b) * p.bt_stride + x.col0 + j] : -1;
             }
         };
-        if (lane == 0) nxt = atomicAdd(p.sched, 1);
-        Work w;
-        decode(__shfl_sync(kFull, nxt, 0), w);
+        Work w, wn;
+        next_work(w);
         load_pages(w);
-        if (lane == 0) nxt = atomicAdd(p.sched, 1);
+        next_work(wn);
+        int ru = 0;  // runs started
         for (int it = 0;; ++it) {
             const int slot = it % kTcNI;
             if (it >= kTcNI && !tc_wait(bar(S::B_IE + slot), ((it / kTcNI) - 1) & 1, p, kWaitNs)) { ok = false; break; }
             TcItem& I = items[slot];
-            if (w.i >= n_items) {
+            if (!w.valid) {
                 if (lane == 0) I.end = 1;
                 __syncwarp();
                 mbar_arrive(bar(S::B_IF + slot));
@@ -360,25 +515,28 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
             }
             bad = __any_sync(kFull, bad);
             if (lane == 0) {
-                I.b = b; I.hk = hk; I.c = w.c; I.nch = w.nch; I.t0 = t0; I.t1 = t1; I.ntiles = ntiles; I.bad = bad;
-                I.end = 0;
+                I.b = b; I.hk = hk; I.slot = w.slot; I.pieces = w.pieces;
+                I.cont = w.cont; I.last = !wn.valid || wn.unit != w.unit;
+                I.t0 = t0; I.t1 = t1; I.ntiles = ntiles; I.bad = bad; I.end = 0;
             }
             __syncwarp();
             mbar_arrive(bar(S::B_IF + slot));
-            // the next item, decoded and its table entries requested while this one streams
-            decode(__shfl_sync(kFull, nxt, 0), w);
-            load_pages(w);
-            if (lane == 0) nxt = atomicAdd(p.sched, 1);
-            // the unit's q rows (two 64-dim halves)
-            const int qb = it & 1;
-            if (it >= 2 && !tc_wait(bar(S::B_QE + qb), ((it >> 1) - 1) & 1, p, kWaitNs)) { ok = false; break; }
-            if (lane == 0) {
-                mbar_arrive_expect_tx(bar(S::B_QF + qb), M * 256);
-                for (int h = 0; h < 2; ++h)
-                    tma_load_3d(sb0 + S::OFF_Q + qb * S::QB + h * 4096, &qmap, 64 * h, hk * p.G, b * p.sq,
-                                bar(S::B_QF + qb), pol);
+            const bool new_run = !w.cont;
+            // the next item's table entries, requested while this one streams
+            load_pages(wn);
+            // a run's q rows (two 64-dim halves)
+            if (new_run) {
+                const int qb = ru & 1;
+                if (ru >= 2 && !tc_wait(bar(S::B_QE + qb), ((ru >> 1) - 1) & 1, p, kWaitNs)) { ok = false; break; }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(bar(S::B_QF + qb), M * 256);
+                    for (int h = 0; h < 2; ++h)
+                        tma_load_3d(sb0 + S::OFF_Q + qb * S::QB + h * 4096, &qmap, 64 * h, hk * p.G, b * p.sq,
+                                    bar(S::B_QF + qb), pol);
+                }
+                ++qiss;
+                ++ru;
             }
-            ++qiss;
             // K/V tiles: lane s < 8 loads stage s (two 8-key groups, 4 KB each)
             for (int k = 0; k < ntiles; ++k, ++t) {
                 const int tok0 = t0 + k * kTcTile, ts = t % kTcNS;
@@ -398,6 +556,8 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
                 ++tiss;
             }
             if (!ok) break;
+            w = wn;
+            next_work(wn);
         }
         if (!ok) {
             // let every issued copy land before the CTA leaves
@@ -409,15 +569,17 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
         // ----------------------------------------------------- S^T = K Q^T
         if (lane == 0) {
             bool ok = true;
-            int t = 0;
+            int t = 0, ru = 0;
             for (int it = 0; ok; ++it) {
                 const int slot = it % kTcNI;
                 if (!mbar_wait(bar(S::B_IF + slot), (it / kTcNI) & 1, p.status)) { ok = false; break; }
                 const TcItem& I = items[slot];
                 if (I.end) break;
-                const int ntiles = I.ntiles, qb = it & 1;
+                const int ntiles = I.ntiles, last = I.last;
+                if (!I.cont) ++ru;
+                const int qb = (ru - 1) & 1;
                 mbar_arrive(bar(S::B_IE + slot));
-                if (!mbar_wait(bar(S::B_QF + qb), (it >> 1) & 1, p.status, p.wait_ns)) { ok = false; break; }
+                if (!I.cont && !mbar_wait(bar(S::B_QF + qb), ((ru - 1) >> 1) & 1, p.status, p.wait_ns)) { ok = false; break; }
                 for (int k = 0; k < ntiles; ++k, ++t) {
                     const int ts = t % kTcNS, sbuf = t & 1;
                     if (!mbar_wait(bar(S::B_TF + ts), (t / kTcNS) & 1, p.status, p.wait_ns)) { ok = false; break; }
@@ -430,7 +592,7 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
                                       tc05::smem_desc(tile + (kk >> 2) * 1024 + (kk & 3) * 32, 16, S::GROUP),
                                       tc05::smem_desc(qt + (kk >> 2) * 4096 + (kk & 3) * 32, 16, 1024), kIdS, kk > 0);
                     tc05::commit(bar(S::B_SF + sbuf));
-                    if (k == ntiles - 1) tc05::commit(bar(S::B_QE + qb));
+                    if (last && k == ntiles - 1) tc05::commit(bar(S::B_QE + qb));
                 }
             }
             if (!ok) raise_status(p, kErrTimeout);
@@ -445,18 +607,21 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
         // K/V slot is released without waiting for the next tile's keys
         if (lane == 0) {
             bool ok = true;
-            int t = 0;
+            int t = 0, ru = 0;
             for (int it = 0; ok; ++it) {
-                const int slot = it % kTcNI, ob = it & 1;
+                const int slot = it % kTcNI;
                 if (!mbar_wait(bar(S::B_IF + slot), (it / kTcNI) & 1, p.status)) { ok = false; break; }
                 const TcItem& I = items[slot];
                 if (I.end) break;
-                const int ntiles = I.ntiles;
+                const int ntiles = I.ntiles, last = I.last, cont = I.cont;
+                if (!cont) ++ru;
+                const int ob = (ru - 1) & 1;
                 mbar_arrive(bar(S::B_IE + slot));
                 for (int k = 0; k < ntiles; ++k, ++t) {
                     const int ts = t % kTcNS;
+                    const bool run_start = !cont && k == 0;
                     if (!mbar_wait(bar(S::B_PF), t & 1, p.status)) { ok = false; break; }
-                    if (k == 0 && it >= 2 && !mbar_wait(bar(S::B_OE + ob), ((it >> 1) - 1) & 1, p.status)) { ok = false; break; }
+                    if (run_start && ru >= 3 && !mbar_wait(bar(S::B_OE + ob), (((ru - 1) >> 1) - 1) & 1, p.status)) { ok = false; break; }
                     tc05::fence_after_sync();
                     const uint32_t tile = sb0 + S::OFF_KV + ts * S::TILE, ptile = sb0 + S::OFF_P;
 #pragma unroll
@@ -464,10 +629,10 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
                         tc05::mma_f16(tmem + 64 + 32 * ob,
                                       tc05::smem_desc(tile + 2 * j * S::GROUP + 2048, 1024, S::GROUP),
                                       tc05::smem_desc(ptile + (j >> 2) * 4096 + (j & 3) * 32, 16, 1024), kIdO,
-                                      !(k == 0 && j == 0));
+                                      !(run_start && j == 0));
                     tc05::commit(bar(S::B_PD));
                     tc05::commit(bar(S::B_TE + ts));
-                    if (k == ntiles - 1) tc05::commit(bar(S::B_OF + ob));
+                    if (last && k == ntiles - 1) tc05::commit(bar(S::B_OF + ob));
                 }
             }
             if (!ok) raise_status(p, kErrTimeout);
@@ -486,10 +651,10 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
         float* gred = red + grp * 2 * RG * 4;
         const uint32_t lane_addr = static_cast<uint32_t>(32 * q4) << 16;
         const float scale2 = p.scale_log2;
-        int nvote = 0, t = 0;
+        int nvote = 0, t = 0, ru = 0;
         float m_used[RG], lp[RG];
         for (int it = 0;; ++it) {
-            const int slot = it % kTcNI, ob = it & 1;
+            const int slot = it % kTcNI;
             const int fail = !tc_wait(bar(S::B_IF + slot), (it / kTcNI) & 1, p, kWaitNs);
             const TcItem& I = items[slot];
             const int end = fail ? 1 : I.end;
@@ -497,13 +662,18 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
                 if (fail) raise_status(p, kErrTimeout);
                 break;
             }
-            const int t0 = I.t0, t1 = I.t1, ntiles = I.ntiles, bad = I.bad;
+            const int t0 = I.t0, t1 = I.t1, ntiles = I.ntiles, bad = I.bad, cont = I.cont, last = I.last;
             const int col0 = page_div(t0, p.pmagic, p.pmshift);
+            if (!cont) {
+                // a new run: fresh statistics
+                ++ru;
 #pragma unroll
-            for (int r = 0; r < RG; ++r) {
-                m_used[r] = -INFINITY;
-                lp[r] = 0.f;
+                for (int r = 0; r < RG; ++r) {
+                    m_used[r] = -INFINITY;
+                    lp[r] = 0.f;
+                }
             }
+            const int ob = (ru - 1) & 1;
             bool abort = false;
             for (int k = 0; k < ntiles; ++k, ++t) {
                 const int sbuf = t & 1, ts = t % kTcNS;
@@ -555,8 +725,8 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
                         m_used[r] = __shfl_sync(kFull, m_new, r);
                         lp[r] *= __shfl_sync(kFull, a_lane, r);
                     }
-                    if (grew && k > 0) {
-                        // O holds the item's earlier tiles: rescale once their P.V has completed
+                    if (grew && (cont || k > 0)) {
+                        // O holds the run's earlier tiles: rescale once their P.V has completed
                         if (tc_wait(bar(S::B_PD), (t - 1) & 1, p, kWaitNs)) {
                             tc05::fence_after_sync();
                             uint32_t o[RG];
@@ -613,13 +783,16 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
                 raise_status(p, kErrTimeout);
                 break;
             }
-            // row statistics for the epilogue: this warp's share of l, and m
-            const float lw = tc_row_reduce16(lp, lane, [](float a, float b2) { return a + b2; });
-            const bool free_ok = it < 2 || tc_wait(bar(S::B_XE + ob), ((it >> 1) - 1) & 1, p, kWaitNs);
-            float* st = stats + ob * 5 * kTcRows;
-            if ((lane & 1) == 0) st[q4 * kTcRows + rbase + (lane >> 1)] = lw;
-            if (q4 == 0 && lane < RG) st[4 * kTcRows + rbase + lane] = tc_pick16(m_used, lane);
-            mbar_arrive(bar(S::B_XF + ob));
+            bool free_ok = true;
+            if (last) {
+                // row statistics of the run for the epilogue: this warp's share of l, and m
+                const float lw = tc_row_reduce16(lp, lane, [](float a, float b2) { return a + b2; });
+                free_ok = ru < 3 || tc_wait(bar(S::B_XE + ob), (((ru - 1) >> 1) - 1) & 1, p, kWaitNs);
+                float* st = stats + ob * 5 * kTcRows;
+                if ((lane & 1) == 0) st[q4 * kTcRows + rbase + (lane >> 1)] = lw;
+                if (q4 == 0 && lane < RG) st[4 * kTcRows + rbase + lane] = tc_pick16(m_used, lane);
+                mbar_arrive(bar(S::B_XF + ob));
+            }
             mbar_arrive(bar(S::B_IE + slot));
             if (!free_ok) {
                 raise_status(p, kErrTimeout);  // the next vote stops the group
@@ -627,24 +800,30 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
         }
     } else {
         // ------------------------------------------------------ epilogue
-        const int q4 = warp & 3, et = tid - 256, d = 32 * q4 + lane;  // TMEM lane of O^T: the head dim
+        const int q4 = warp & 3, d = 32 * q4 + lane;  // TMEM lane of O^T: the head dim
         const uint32_t lane_addr = static_cast<uint32_t>(32 * q4) << 16;
         int* evotes = votes + 16;
-        int nvote = 0;
+        int nvote = 0, er = 0;  // er: runs written
         for (int it = 0;; ++it) {
-            const int slot = it % kTcNI, ob = it & 1;
+            const int slot = it % kTcNI, ob = er & 1;
             int fail = !tc_wait(bar(S::B_IF + slot), (it / kTcNI) & 1, p, kWaitNs);
             const TcItem& I = items[slot];
-            const int end = fail ? 1 : I.end;
-            if (!end) {
-                fail |= !tc_wait(bar(S::B_XF + ob), (it >> 1) & 1, p, kWaitNs);
-                fail |= !tc_wait(bar(S::B_OF + ob), (it >> 1) & 1, p, kWaitNs);
+            const int end = fail ? 1 : I.end, last = end ? 0 : I.last;
+            if (last) {
+                fail |= !tc_wait(bar(S::B_XF + ob), (er >> 1) & 1, p, kWaitNs);
+                fail |= !tc_wait(bar(S::B_OF + ob), (er >> 1) & 1, p, kWaitNs);
             }
             if (tc_vote(evotes, 2, nvote, q4, lane, (fail ? 2 : 0) | (end ? 1 : 0))) {
                 if (fail) raise_status(p, kErrTimeout);
                 break;
             }
-            const int b = I.b, hk = I.hk, c = I.c, nch = I.nch;
+            if (!last) {
+                // the run goes on in the next item
+                mbar_arrive(bar(S::B_IE + slot));
+                continue;
+            }
+            ++er;
+            const int b = I.b, hk = I.hk, pslot = I.slot, np = I.pieces;
             // O^T of the item (this thread's head dim, 32 rows); l and m per row
             // are read from the softmax's statistics as they are needed
             tc05::fence_after_sync();
@@ -658,7 +837,7 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
             const long long unit = static_cast<long long>(b) * Hkv + hk;
             const long long row0 = static_cast<long long>(b) * p.sq * p.Hq + hk * p.G;  // output row of query row 0
             auto out_row = [&](int r) { return row0 + static_cast<long long>(r / p.G) * p.Hq + r % p.G; };
-            if (nch == 1) {
+            if (np == 1) {
                 int i = 0, g = 0;
 #pragma unroll
                 for (int r = 0; r < 32; ++r) {
@@ -677,9 +856,9 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
                 }
                 mbar_arrive(bar(S::B_XE + ob));
             } else {
-                // this chunk's partial (normalised O, LSE in log2 units), merged
-                // by the merge kernel after this launch
-                const long long slot2 = unit * p.max_splits + c;
+                // this run's partial (normalised O, LSE in log2 units); the CTA
+                // that completes the unit's last piece merges them
+                const long long slot2 = unit * p.max_splits + pslot;
                 float* po = p.part_out + slot2 * kTcRows * 128;
 #pragma unroll
                 for (int r = 0; r < 32; ++r) {
@@ -692,6 +871,16 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
                     __stcg(p.part_lse + slot2 * kTcRows + d, l > 0.f ? st[4 * kTcRows + d] + __log2f(l) : -INFINITY);
                 }
                 mbar_arrive(bar(S::B_XE + ob));
+                // publish the piece: every thread's stores, then one arrival
+                __threadfence();
+                tc_group_sync(2);
+                if (q4 == 0 && lane == 0) votes[24] = atomicAdd(p.counters + unit, 1);
+                tc_group_sync(2);
+                if (votes[24] == np - 1) {
+                    __threadfence();
+                    tc_merge_unit(p, unit, row0, np, q4, lane);
+                    if (q4 == 0 && lane == 0) p.counters[unit] = 0;  // every piece has arrived: ready for the next call
+                }
             }
             mbar_arrive(bar(S::B_IE + slot));
         }
@@ -703,15 +892,6 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
     if (warp == 13) {
         tc05::fence_after_sync();
         tc05::dealloc(tmem, 128);
-    }
-    if (tid == 0) {
-        // the last CTA to finish resets the queue for the next call
-        __threadfence();
-        const int prev = atomicAdd(p.sched + 32, 1);
-        if (prev == static_cast<int>(gridDim.x) - 1) {
-            atomicExch(p.sched, 0);
-            atomicExch(p.sched + 32, 0);
-        }
     }
 }
 

@@ -38,6 +38,7 @@ def _check(case, tol=None, batch_index=None, **kw):
 
 LENS = [1, 15, 16, 17, 200, 1000, 777, 64, 0, 333]
 B50_LENS = [1000 + (i * 397) % 1049 for i in range(50)]
+SHORT40 = [(i * 211) % 900 for i in range(40)]  # 0-899 keys, one empty request
 
 SMALL = {
     # name: paged_case kwargs, call kwargs
@@ -54,6 +55,13 @@ SMALL = {
     # warp pairs over 50 requests of 1000-2048 keys
     "bf16_sq8_b50": (dict(seq_lens=B50_LENS, sq=8), dict()),
     "bf16_sq8_b50_window300_causal": (dict(seq_lens=B50_LENS, sq=8, window=300, causal=True), dict()),
+    # tcgen05 kernel with more chunks than SMs: equal tile shares that cut
+    # chunks (also one-chunk units), a chunk that is not a whole number of
+    # tiles, short and empty requests
+    "bf16_sq8_b50_window700_share": (dict(seq_lens=B50_LENS, sq=8, window=700), dict()),
+    "bf16_sq8_b50_chunk480_share": (dict(seq_lens=B50_LENS, sq=8), dict(chunk_tokens=480)),
+    "fp16_sq8_b40_short_chunk256_share": (dict(seq_lens=SHORT40, sq=8, dtype="fp16", scales=(1.3, 0.7, 0.9)),
+                                          dict(chunk_tokens=256)),
     "bf16_mha_g1": (dict(seq_lens=LENS, num_heads=8, num_kv_heads=8), dict(chunk_tokens=48)),
     "bf16_g2_sq1": (dict(seq_lens=LENS, num_heads=4, num_kv_heads=2), dict()),
     "bf16_g8": (dict(seq_lens=LENS, num_heads=64, num_kv_heads=8), dict(chunk_tokens=96)),
