@@ -275,8 +275,9 @@ pkd_status get_map(CUtensorMap& out, const void* base, int rank, uint64_t d0, ui
 // half_rows the box is {one chunk, 8 rows, one chunk}: one copy per chunk
 // fills the first 8 rows of that chunk's 16-row slot.
 // Boxes of the stage map: a whole 16-key stage (every chunk), its first 8
-// rows of one chunk, or the tcgen05 kernel's group: 8 rows of
-// kTcBoxChunks chunks.
+// rows of one chunk, or the tcgen05 kernel's stage: a 4-D view {chunk
+// elements, 8 rows, chunk, 8-row group} whose box {all, 8, all, 2} lands a
+// 16-key stage as two 8-row groups, each holding every chunk of its rows.
 enum StageBox { kStageFull = 0, kStageHalfRows = 1, kStageTcGroup = 2 };
 
 pkd_status get_stage_map(CUtensorMap& out, const void* cache, uint64_t rows, int row_bytes, pkd_dtype dt,
@@ -285,7 +286,7 @@ pkd_status get_stage_map(CUtensorMap& out, const void* cache, uint64_t rows, int
     MapKey k;
     std::memset(&k, 0, sizeof k);
     k.base = cache; k.d0 = 128 / elt; k.d1 = rows; k.d2 = row_bytes / 128; k.s1 = row_bytes; k.s2 = 128;
-    k.rank = mode == kStageHalfRows ? 108 : mode == kStageTcGroup ? 120 + pkd::kTcBoxChunks : 103; k.dtype = dt;
+    k.rank = mode == kStageHalfRows ? 108 : mode == kStageTcGroup ? 140 : 103; k.dtype = dt;
     MapCache& c = map_cache();
     {
         std::lock_guard<std::mutex> g(c.mu);
@@ -300,14 +301,25 @@ pkd_status get_stage_map(CUtensorMap& out, const void* cache, uint64_t rows, int
     const CUtensorMapDataType t = dt == PKD_BF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                   : dt == PKD_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                    : CU_TENSOR_MAP_DATA_TYPE_UINT8;
-    cuuint64_t dims[3] = {k.d0, k.d1, k.d2};
-    cuuint64_t strides[2] = {k.s1, k.s2};
-    cuuint32_t box[3] = {(cuuint32_t)(128 / elt), (cuuint32_t)(mode == kStageFull ? pkd::kStageTok : pkd::kStageTok / 2),
-                         (cuuint32_t)(mode == kStageHalfRows ? 1 : mode == kStageTcGroup ? pkd::kTcBoxChunks : row_bytes / 128)};
-    cuuint32_t estr[3] = {1, 1, 1};
     CUtensorMap m;
-    CUresult r = enc(&m, t, 3, const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r;
+    if (mode == kStageTcGroup) {
+        // rows is a multiple of 16 (page_size is)
+        cuuint64_t dims[4] = {k.d0, 8, k.d2, k.d1 / 8};
+        cuuint64_t strides[3] = {k.s1, k.s2, 8 * k.s1};
+        cuuint32_t box[4] = {(cuuint32_t)(128 / elt), 8, (cuuint32_t)(row_bytes / 128), 2};
+        cuuint32_t estr[4] = {1, 1, 1, 1};
+        r = enc(&m, t, 4, const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        cuuint64_t dims[3] = {k.d0, k.d1, k.d2};
+        cuuint64_t strides[2] = {k.s1, k.s2};
+        cuuint32_t box[3] = {(cuuint32_t)(128 / elt), (cuuint32_t)(mode == kStageFull ? pkd::kStageTok : pkd::kStageTok / 2),
+                             (cuuint32_t)(mode == kStageHalfRows ? 1 : row_bytes / 128)};
+        cuuint32_t estr[3] = {1, 1, 1};
+        r = enc(&m, t, 3, const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
     if (r != CUDA_SUCCESS) return fail(PKD_ECUDA, "cuTensorMapEncodeTiled (stage map) failed (CUresult %d)", (int)r);
     {
         std::lock_guard<std::mutex> g(c.mu);

@@ -20,15 +20,17 @@
 //                    tcgen05.ld of its 32 scores, online softmax per query
 //                    row in fp32 whose reference maximum moves only when a
 //                    row's maximum grows by more than 2^8 (then O and l are
-//                    rescaled), P written to shared memory in the operand
-//                    type.
+//                    rescaled), P written in the operand type over the
+//                    tile's K in shared memory (dead once S is computed), so
+//                    that each slot carries its own P.
 //   O^T += V^T P^T   M = 128 dims, N = 32 rows, K = 128 keys: A = the V tile
 //                    read MN-major, B = P (K-major); O^T accumulates in TMEM
 //                    over the run's tiles.
-// A tile lands as sixteen 4 KB groups of 8 keys, one TMA copy each, every
-// group holding the four 128-byte chunks of its rows (K dims 0-63, K 64-127,
-// V 0-63, V 64-127; 1 KB each, 128-byte swizzle): both products then see
-// rows at a uniform 4 KB stride, and a 16-key stage takes two copies.
+// A tile lands as sixteen 4 KB groups of 8 keys, every group holding the
+// four 128-byte chunks of its rows (K dims 0-63, K 64-127, V 0-63, V 64-127;
+// 1 KB each, 128-byte swizzle), so that both products see rows at a uniform
+// 4 KB stride; a 16-key stage (two groups, contiguous in the page) is one
+// TMA copy of a 4-D view of the cache.
 // Warp roles: warps 0-7 run the softmax in two groups of four, each group
 // taking 16 of the 32 query rows, warps 8-11 the epilogue (read O^T,
 // normalise, write out and LSE -- or, for a unit split into several runs,
@@ -50,7 +52,6 @@ namespace pkd {
 
 constexpr int kTcTile = 128;      // keys per tile: the M of S^T = K Q^T
 constexpr int kTcRows = 32;       // query rows per unit, padded: the N of both products
-constexpr int kTcBoxChunks = 4;  // 128-byte chunks per TMA group copy: K and V
 constexpr int kTcNS = 3;          // K/V tile ring
 constexpr int kTcNI = 4;          // work-item ring
 constexpr int kTcMaxChunk = 2048; // keys per chunk at most
@@ -94,22 +95,23 @@ struct TcShape {
     static constexpr int GROUP = 4096;                 // 8 keys: K 0-63 | K 64-127 | V 0-63 | V 64-127
     static constexpr int TILE = (kTcTile / 8) * GROUP; // 64 KB
     static constexpr int QB = kTcRows * 256;           // q rows: two regions of 32 x 128 bytes
-    static constexpr int PB = kTcRows * kTcTile * 2;   // P: keys 0-63, then 64-127, 32 rows each
+    // P of a tile goes where its K was (dead once S is computed): 8-row group
+    // g of key half h in the first 1 KB of the slot's 4 KB group 4h + g
     static constexpr int OFF_KV = 0;
     static constexpr int OFF_Q = OFF_KV + kTcNS * TILE;
-    static constexpr int OFF_P = OFF_Q + 2 * QB;
-    static constexpr int OFF_ITEM = OFF_P + PB;
+    static constexpr int OFF_ITEM = OFF_Q + 2 * QB;
     static constexpr int OFF_STAT = OFF_ITEM + kTcNI * static_cast<int>(sizeof(TcItem));  // [2][4 warps + m][32]
     static constexpr int OFF_RED = OFF_STAT + 2 * 5 * kTcRows * 4;  // float [2][32 rows][4 warps]
     static constexpr int OFF_VOTE = OFF_RED + 2 * kTcRows * 4 * 4;  // int votes [2][4] per group; [24]: arrivals
     static constexpr int OFF_PREF = OFF_VOTE + 128;                 // int [kTcMaxBatch + 1]: work prefix
     static constexpr int OFF_LENS = OFF_PREF + (kTcMaxBatch + 1) * 4;  // int [kTcMaxBatch]: clamped lengths
     static constexpr int OFF_BAR = (OFF_LENS + kTcMaxBatch * 4 + 7) & ~7;
-    // barriers: K/V full/empty, q full/empty, S full/empty, P full, P.V done,
-    // O full/free, stats full/free, item full/empty, final drain
+    // barriers: K/V full/empty (the empty one also says P.V is done), q
+    // full/empty, S full/empty, P full (per slot), O full/free, stats
+    // full/free, item full/empty, final drain
     static constexpr int B_TF = 0, B_TE = B_TF + kTcNS, B_QF = B_TE + kTcNS, B_QE = B_QF + 2;
-    static constexpr int B_SF = B_QE + 2, B_SE = B_SF + 2, B_PF = B_SE + 2, B_PD = B_PF + 1;
-    static constexpr int B_OF = B_PD + 1, B_OE = B_OF + 2, B_XF = B_OE + 2, B_XE = B_XF + 2;
+    static constexpr int B_SF = B_QE + 2, B_SE = B_SF + 2, B_PF = B_SE + 2;
+    static constexpr int B_OF = B_PF + kTcNS, B_OE = B_OF + 2, B_XF = B_OE + 2, B_XE = B_XF + 2;
     static constexpr int B_IF = B_XE + 2, B_IE = B_IF + kTcNI, B_DR = B_IE + kTcNI, NBAR = B_DR + 2;
     static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_TMEM + 16 + 1024;
@@ -323,8 +325,7 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
             mbar_init(bar(S::B_XF + i), 256);
             mbar_init(bar(S::B_XE + i), 128);
         }
-        mbar_init(bar(S::B_PF), 256);
-        mbar_init(bar(S::B_PD), 1);
+        for (int i = 0; i < kTcNS; ++i) mbar_init(bar(S::B_PF + i), 256);
         for (int i = 0; i < kTcNI; ++i) {
             mbar_init(bar(S::B_IF + i), 32);
             mbar_init(bar(S::B_IE + i), 2 + 256 + 128);  // both MMA threads, softmax and epilogue groups
@@ -537,7 +538,7 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
                 ++qiss;
                 ++ru;
             }
-            // K/V tiles: lane s < 8 loads stage s (two 8-key groups, 4 KB each)
+            // K/V tiles: lane s < 8 loads stage s (16 keys: two 4 KB groups, one copy)
             for (int k = 0; k < ntiles; ++k, ++t) {
                 const int tok0 = t0 + k * kTcTile, ts = t % kTcNS;
                 if (t >= kTcNS && !tc_wait(bar(S::B_TE + ts), ((t / kTcNS) - 1) & 1, p, kWaitNs)) { ok = false; break; }
@@ -548,10 +549,9 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
                 if (lane == 0) mbar_arrive_expect_tx(bar(S::B_TF + ts), __popc(loaded) * 2 * S::GROUP);
                 __syncwarp();
                 if (pg >= 0) {
-                    const int row = (pg * Hkv + hk) * p.P + (tok - col * p.P);
+                    const int row = (pg * Hkv + hk) * p.P + (tok - col * p.P);  // a multiple of 16
                     const uint32_t dst = sb0 + S::OFF_KV + ts * S::TILE + 2 * lane * S::GROUP;
-                    tma_load_3d(dst, &kvmap, 0, row, 0, bar(S::B_TF + ts), pol);
-                    tma_load_3d(dst + S::GROUP, &kvmap, 0, row + 8, 0, bar(S::B_TF + ts), pol);
+                    tma_load_4d(dst, &kvmap, 0, 0, 0, row >> 3, bar(S::B_TF + ts), pol);
                 }
                 ++tiss;
             }
@@ -620,17 +620,16 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
                 for (int k = 0; k < ntiles; ++k, ++t) {
                     const int ts = t % kTcNS;
                     const bool run_start = !cont && k == 0;
-                    if (!mbar_wait(bar(S::B_PF), t & 1, p.status)) { ok = false; break; }
+                    if (!mbar_wait(bar(S::B_PF + ts), (t / kTcNS) & 1, p.status)) { ok = false; break; }
                     if (run_start && ru >= 3 && !mbar_wait(bar(S::B_OE + ob), (((ru - 1) >> 1) - 1) & 1, p.status)) { ok = false; break; }
                     tc05::fence_after_sync();
-                    const uint32_t tile = sb0 + S::OFF_KV + ts * S::TILE, ptile = sb0 + S::OFF_P;
+                    const uint32_t tile = sb0 + S::OFF_KV + ts * S::TILE;
 #pragma unroll
                     for (int j = 0; j < kTcTile / 16; ++j)
                         tc05::mma_f16(tmem + 64 + 32 * ob,
                                       tc05::smem_desc(tile + 2 * j * S::GROUP + 2048, 1024, S::GROUP),
-                                      tc05::smem_desc(ptile + (j >> 2) * 4096 + (j & 3) * 32, 16, 1024), kIdO,
-                                      !(run_start && j == 0));
-                    tc05::commit(bar(S::B_PD));
+                                      tc05::smem_desc(tile + (j >> 2) * 4 * S::GROUP + (j & 3) * 32, 16, S::GROUP),
+                                      kIdO, !(run_start && j == 0));
                     tc05::commit(bar(S::B_TE + ts));
                     if (last && k == ntiles - 1) tc05::commit(bar(S::B_OF + ob));
                 }
@@ -726,8 +725,9 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
                         lp[r] *= __shfl_sync(kFull, a_lane, r);
                     }
                     if (grew && (cont || k > 0)) {
-                        // O holds the run's earlier tiles: rescale once their P.V has completed
-                        if (tc_wait(bar(S::B_PD), (t - 1) & 1, p, kWaitNs)) {
+                        // O holds the run's earlier tiles: rescale once their P.V has
+                        // completed (the previous tile's slot released)
+                        if (tc_wait(bar(S::B_TE + (t - 1) % kTcNS), ((t - 1) / kTcNS) & 1, p, kWaitNs)) {
                             tc05::fence_after_sync();
                             uint32_t o[RG];
                             tc05::ld_32x32b_x16(tmem + lane_addr + 64 + 32 * ob + rbase, o);
@@ -742,23 +742,21 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
                         }
                     }
                 }
-                // P (rows past M and keys outside the chunk are 0), once the previous
-                // tile's P.V has read the buffer
+                // P (rows past M and keys outside the chunk are 0), over the tile's K
                 float pr[RG];
 #pragma unroll
                 for (int r = 0; r < RG; ++r) {
                     pr[r] = m_used[r] == -INFINITY ? 0.f : fast_exp2(x[r] - m_used[r]);
                     lp[r] += pr[r];
                 }
-                if (t >= 1 && !tc_wait(bar(S::B_PD), (t - 1) & 1, p, kWaitNs)) abort = true;
-                uint8_t* ptile = smem + S::OFF_P + (key >> 6) * 4096;
+                uint8_t* ptile = smem + S::OFF_KV + ts * S::TILE + (key >> 6) * 4 * S::GROUP;
                 const int kc = (key & 63) >> 3, kb2 = (key & 7) * 2;
 #pragma unroll
                 for (int r = 0; r < RG; ++r) {
                     const int row = rbase + r;
                     const uint32_t h = pack2<kBF16>(pr[r], 0.f);
-                    *reinterpret_cast<uint16_t*>(ptile + row * 128 + (((kc ^ (row & 7)) << 4) | kb2)) =
-                        static_cast<uint16_t>(h & 0xffffu);
+                    *reinterpret_cast<uint16_t*>(ptile + (row >> 3) * S::GROUP + (row & 7) * 128 +
+                                                 (((kc ^ (row & 7)) << 4) | kb2)) = static_cast<uint16_t>(h & 0xffffu);
                 }
                 if (grp == 0 && __any_sync(kFull, !valid)) {
                     // keys outside the chunk (or on a skipped page) get P = 0; their V
@@ -777,7 +775,7 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
                 }
                 fence_proxy_async();      // P and zeroed rows are read by the tensor cores
                 tc05::fence_before_sync();
-                mbar_arrive(bar(S::B_PF));
+                mbar_arrive(bar(S::B_PF + ts));
             }
             if (tc_vote(gvotes, gid, nvote, q4, lane, abort ? 2 : 0) & 2) {
                 raise_status(p, kErrTimeout);
