@@ -136,7 +136,9 @@ pkd_status make_plan(int B, int sq, int Hq, int Hkv, int D, int P, int max_kv_le
         if (chunk_tokens > 0 && chunk_tokens % P != 0)
             return fail(PKD_EINVAL, "chunk_tokens %d must be a multiple of page_size %d", chunk_tokens, P);
         // automatic: a quarter of the longest visible range in whole tiles,
-        // 1024-2048 keys
+        // 1024-2048 keys, when every chunk has a CTA of its own; when CTAs
+        // take tile shares, chunks of the largest size (fewer items per run;
+        // at most as many pieces per unit as the plan's chunks + 1)
         int auto_chunk = (pl.max_vis / 4 + pkd::kTcTile - 1) / pkd::kTcTile * pkd::kTcTile;
         if (auto_chunk < kTcChunkMin) auto_chunk = kTcChunkMin;
         if (auto_chunk > pkd::kTcMaxChunk) auto_chunk = pkd::kTcMaxChunk;
@@ -493,6 +495,7 @@ pkd_status pkd_paged_decode(const void* q, pkd_dtype q_dtype, const void* kv_cac
     p.P = page_size;
     p.max_kv_len = max_kv_len;
     p.chunk = pl.chunk;
+    p.chunk_share = chunk_tokens > 0 ? chunk_tokens : pkd::kTcMaxChunk;
     p.max_splits = pl.max_splits;
     p.window = window > 0 ? window : 0;
     p.causal = (flags & PKD_FLAG_CAUSAL) ? 1 : 0;

@@ -31,6 +31,7 @@ struct DecodeParams {
     long long num_pages;
     int B, sq, Hq, Hkv, G, M, P;
     int max_kv_len, chunk, max_splits, window, causal;
+    int chunk_share;             // tcgen05 kernel: chunk when CTAs take tile shares
     int out_dtype;               // 0 bf16, 1 fp16, 3 fp32
     uint32_t pmagic;             // tok / P == (tok * pmagic) >> pmshift for 0 <= tok < 2^31
     int pmshift;

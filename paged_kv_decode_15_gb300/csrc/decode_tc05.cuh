@@ -306,7 +306,8 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
     int* lens = reinterpret_cast<int*>(smem + S::OFF_LENS);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + S::OFF_TMEM);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int Hkv = p.Hkv, M = p.M, C = p.chunk;
+    const int Hkv = p.Hkv, M = p.M;
+    int C = p.chunk;  // warp 12: the chunk of the launch's mode
     auto bar = [&](int i) { return smem_u32(bars + i); };
 
     // ------------------------------------------------------------ set-up
@@ -339,7 +340,7 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
         tc05::relinquish_alloc_permit();
     }
     // warp 12: the launch's work -- chunks (item mode, no more than CTAs) or
-    // tiles (share mode) of all requests -- and its prefix per request in pref
+    // tiles of the share mode's chunks -- and its prefix per request in pref
     bool by_item = true;
     int total = 0;
     if (warp == 12) {
@@ -348,10 +349,9 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
             const int b = b0 + lane;
             int ni = 0, nt = 0;
             if (b < p.B) {
-                const int L = clamp_len(p, b, true);
-                const TcChunks ch = tc_chunks(L - visible_lo(p, L), C);
-                ni = ch.n * Hkv;
-                nt = ch.tiles * Hkv;
+                const int L = clamp_len(p, b, true), vis = L - visible_lo(p, L);
+                ni = tc_chunks(vis, p.chunk).n * Hkv;
+                nt = tc_chunks(vis, p.chunk_share).tiles * Hkv;
                 lens[b] = L;
             }
             n_items += __reduce_add_sync(kFull, ni);
@@ -359,6 +359,7 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
         }
         by_item = n_items <= static_cast<int>(gridDim.x);
         total = by_item ? n_items : n_tiles;
+        C = by_item ? p.chunk : p.chunk_share;
         int run = 0;
         for (int b0 = 0; b0 < p.B; b0 += 32) {
             const int b = b0 + lane;
