@@ -143,7 +143,7 @@ pkd_status pkd_workspace_check(void* workspace, size_t workspace_bytes, void* st
  * chunk_tokens keys (0: chosen by the library: about 2048 CTAs, chunks of at
  * most 4096 keys -- 32 chunks for 64 (request, kv head) units of 131,072
  * keys).  16-bit query blocks of M = sq * num_heads / num_kv_heads = 17-32
- * rows with head_dim 128, no causal mask and batch <= 512 run instead on a
+ * rows with head_dim 128 and batch <= 512 (dense or causal) run instead on a
  * persistent kernel with one CTA per SM on the tcgen05 tensor cores: chunks
  * of at most chunk_tokens keys (0: a quarter of the longest visible range in
  * whole 128-key tiles, between 1024 and 2048 keys; 2048 at most), equal

@@ -95,10 +95,10 @@ pkd_status make_plan(int B, int sq, int Hq, int Hkv, int D, int P, int max_kv_le
     }
     pl.flat = !pl.bal && B <= pkd::kFlatMaxBatch && !(flags & PKD_FLAG_GRID) &&
               ((flags & PKD_FLAG_FLAT) || flat_default);
-    // 16-bit query blocks of 17-32 rows without a causal mask: the tcgen05
-    // kernel (query_block_sq8: see the kernel-choice table of the design notes)
+    // 16-bit query blocks of 17-32 rows, dense or causal: the tcgen05 kernel
+    // (query_block_sq8: see the kernel-choice table of the design notes)
     pl.tc = !pl.bal && !pl.flat && (kv == PKD_BF16 || kv == PKD_FP16) && D == 128 && sq * (Hq / Hkv) > 16 &&
-            sq * (Hq / Hkv) <= 32 && B <= pkd::kTcMaxBatch && !(flags & (PKD_FLAG_GRID | PKD_FLAG_FMA | PKD_FLAG_CAUSAL)) &&
+            sq * (Hq / Hkv) <= 32 && B <= pkd::kTcMaxBatch && !(flags & (PKD_FLAG_GRID | PKD_FLAG_FMA)) &&
             (chunk_tokens <= 0 || chunk_tokens <= pkd::kTcMaxChunk);
     if (kv == PKD_FP8_E4M3 && (flags & PKD_FLAG_FMA)) {
         if (M > 8) return fail(PKD_EUNSUPPORTED, "fp8 on CUDA cores supports sq*num_heads/num_kv_heads <= 8 (got %d)", M);

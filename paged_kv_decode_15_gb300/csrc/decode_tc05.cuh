@@ -1,5 +1,7 @@
 // Paged decode of query blocks with 17-32 rows per kv head (M = sq * Hq/Hkv)
-// on the 5th-generation tensor cores, accumulators in tensor memory (TMEM).
+// on the 5th-generation tensor cores, accumulators in tensor memory (TMEM);
+// dense or causal (each query token sees the keys up to its own position,
+// within the window).
 //
 // One persistent CTA per SM.  A request's visible keys are cut into chunks
 // of at most `chunk` keys (whole 128-key tiles where the chunk allows).
@@ -65,9 +67,9 @@ constexpr float kTcRescale = 8.f; // log2 units: P stays below 2^8 between resca
 // cont: the item continues the previous item's run (same unit, same
 // accumulators); last: the run ends with it (the epilogue follows); slot: the
 // run's partial slot in its unit; pieces: the unit's runs (1: this run is
-// the whole unit).
+// the whole unit); L: the request's length (for the causal mask).
 struct TcItem {
-    int b, hk, slot, pieces, cont, last, t0, t1, ntiles, bad, end, pad[5];
+    int b, hk, slot, pieces, cont, last, t0, t1, ntiles, bad, end, L, pad[4];
     int pages[kTcItemPages];      // table columns t0/P ..; -1: outside the pool (keys skipped)
 };
 
@@ -429,7 +431,7 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
         int cur = by_item ? me : static_cast<int>(min(static_cast<long long>(total), static_cast<long long>(me) * share));
         const int stop = by_item ? min(total, me + 1) : min(total, cur + share);
         struct Work {
-            int b, hk, unit, slot, pieces, t0, t1, ntiles, col0, npg;
+            int b, hk, unit, slot, pieces, t0, t1, ntiles, col0, npg, L;
             bool valid, cont;
         };
         int prev_unit = -1;
@@ -466,6 +468,7 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
             const int cs = lo + c * ch.len, ce = min(cs + ch.len, L);
             x.b = lo_b;
             x.hk = hk;
+            x.L = L;
             x.unit = lo_b * Hkv + hk;
             x.t0 = cs + k0 * kTcTile;
             x.t1 = min(cs + k1 * kTcTile, ce);
@@ -517,7 +520,7 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
             }
             bad = __any_sync(kFull, bad);
             if (lane == 0) {
-                I.b = b; I.hk = hk; I.slot = w.slot; I.pieces = w.pieces;
+                I.b = b; I.hk = hk; I.slot = w.slot; I.pieces = w.pieces; I.L = w.L;
                 I.cont = w.cont; I.last = !wn.valid || wn.unit != w.unit;
                 I.t0 = t0; I.t1 = t1; I.ntiles = ntiles; I.bad = bad; I.end = 0;
             }
@@ -663,6 +666,9 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
                 break;
             }
             const int t0 = I.t0, t1 = I.t1, ntiles = I.ntiles, bad = I.bad, cont = I.cont, last = I.last;
+            // causal: query token i = row / G sits at L - sq + i and sees keys up
+            // to it (and, with a window, from window - 1 before it on)
+            const int first_pos = I.L - p.sq;
             const int col0 = page_div(t0, p.pmagic, p.pmshift);
             if (!cont) {
                 // a new run: fresh statistics
@@ -680,6 +686,13 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
                 const int tok0 = t0 + k * kTcTile;
                 const int nvalid = min(kTcTile, t1 - tok0);
                 bool valid = key < nvalid;
+                // causal: this key is visible to the rows [rmin, rmax) of the group
+                int rmin = 0, rmax = RG;
+                if (p.causal) {
+                    const int d = tok0 + key - first_pos;  // first token that sees the key
+                    rmin = d * p.G - rbase;
+                    if (p.window > 0) rmax = (d + p.window) * p.G - rbase;
+                }
                 if (bad && valid) valid = I.pages[page_div(tok0 + key, p.pmagic, p.pmshift) - col0] >= 0;
                 float x[RG];
                 const bool got = tc_wait(bar(S::B_SF + sbuf), (t >> 1) & 1, p, kWaitNs);
@@ -692,7 +705,8 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
                     mbar_arrive(bar(S::B_SE + sbuf));
 #pragma unroll
                     for (int r = 0; r < RG; ++r)
-                        x[r] = (valid && rbase + r < M) ? __uint_as_float(sr[r]) * scale2 : -INFINITY;
+                        x[r] = (valid && rbase + r < M && r >= rmin && r < rmax) ? __uint_as_float(sr[r]) * scale2
+                                                                                  : -INFINITY;
                 } else {
 #pragma unroll
                     for (int r = 0; r < RG; ++r) x[r] = -INFINITY;

@@ -58,16 +58,17 @@ def test_workspace_plan_is_a_host_function(lib):
     # ... fp8 caches too ...
     assert pkd.workspace_size(64, 1, 32, 8, 128, 16, 4096, pkd.FP8_E4M3) == \
         pkd.workspace_size(64, 1, 32, 8, 128, 16, 4096, pkd.FP8_E4M3, flags=pkd.FLAG_GRID)
-    # ... 16-bit M > 16 without a causal mask takes the tcgen05 kernel: chunks
+    # ... 16-bit M > 16 (dense or causal) takes the tcgen05 kernel: chunks
     # of at most 2048 keys, and a unit of n chunks in at most n + 1 pieces
     # (CTA shares at least a chunk long), a partial slot of 32 rows each ...
     w = pkd.workspace_size(64, 8, 32, 8, 128, 16, 8192, pkd.BF16)
     assert 512 * 5 * 32 * 128 * 4 <= w < 512 * 6 * 32 * 128 * 4
     assert w == pkd.workspace_size(64, 8, 32, 8, 128, 16, 8192, pkd.BF16, chunk_tokens=2048)
     assert w < pkd.workspace_size(64, 8, 32, 8, 128, 16, 8192, pkd.BF16, chunk_tokens=1024)
-    # ... causal blocks and forced grids keep the warp-pair kernel (as few chunks
-    # as the 4096-key limit allows: 8192 keys -> 2 chunks -> partials [512, 2, 32, 128])
-    g = pkd.workspace_size(64, 8, 32, 8, 128, 16, 8192, pkd.BF16, flags=pkd.FLAG_CAUSAL)
+    assert w == pkd.workspace_size(64, 8, 32, 8, 128, 16, 8192, pkd.BF16, flags=pkd.FLAG_CAUSAL)
+    # ... forced grids keep the warp-pair kernel (as few chunks as the 4096-key
+    # limit allows: 8192 keys -> 2 chunks -> partials [512, 2, 32, 128])
+    g = pkd.workspace_size(64, 8, 32, 8, 128, 16, 8192, pkd.BF16, flags=pkd.FLAG_CAUSAL | pkd.FLAG_GRID)
     assert g == pkd.workspace_size(64, 8, 32, 8, 128, 16, 8192, pkd.BF16, chunk_tokens=4096, flags=pkd.FLAG_GRID)
     assert 512 * 2 * 32 * 128 * 4 <= g < 512 * 3 * 32 * 128 * 4
     # ... while fp8 with M > 16 stays on the flat partition whatever the lengths
@@ -166,7 +167,10 @@ def test_kernel_name_follows_the_plan(lib):
     assert pkd.kernel_name(8, 1, 32, 8, 128, 16, 4096, pkd.BF16) == "chunked grid, tensor cores"
     assert pkd.kernel_name(8, 8, 32, 8, 128, 16, 4096, pkd.BF16) == "persistent tcgen05 kernel, TMEM accumulators"
     assert pkd.kernel_name(8, 8, 32, 8, 128, 16, 4096, pkd.FP16) == "persistent tcgen05 kernel, TMEM accumulators"
-    assert pkd.kernel_name(8, 8, 32, 8, 128, 16, 4096, pkd.BF16, flags=pkd.FLAG_CAUSAL) == "chunked grid, tensor cores"
+    assert pkd.kernel_name(8, 8, 32, 8, 128, 16, 4096, pkd.BF16, flags=pkd.FLAG_CAUSAL) == \
+        "persistent tcgen05 kernel, TMEM accumulators"
+    assert pkd.kernel_name(8, 8, 32, 8, 128, 16, 4096, pkd.BF16, flags=pkd.FLAG_CAUSAL | pkd.FLAG_GRID) == \
+        "chunked grid, tensor cores"
     assert pkd.kernel_name(8, 8, 32, 8, 128, 16, 4096, pkd.BF16, flags=pkd.FLAG_GRID) == "chunked grid, tensor cores"
     assert pkd.kernel_name(8, 8, 32, 8, 64, 16, 4096, pkd.BF16) == "chunked grid, tensor cores"
     assert pkd.kernel_name(8, 8, 32, 8, 128, 16, 8192, pkd.BF16, chunk_tokens=4096) == "chunked grid, tensor cores"

@@ -62,6 +62,11 @@ SMALL = {
     "bf16_sq8_b50_chunk480_share": (dict(seq_lens=B50_LENS, sq=8), dict(chunk_tokens=480)),
     "fp16_sq8_b40_short_chunk256_share": (dict(seq_lens=SHORT40, sq=8, dtype="fp16", scales=(1.3, 0.7, 0.9)),
                                           dict(chunk_tokens=256)),
+    # causal blocks of 32 rows on the tcgen05 kernel: per-row masks across
+    # shares and runs, with and without a window
+    "fp16_sq8_b50_causal_share": (dict(seq_lens=B50_LENS, sq=8, dtype="fp16", causal=True), dict()),
+    "bf16_sq8_b50_causal_window700_chunk480": (dict(seq_lens=B50_LENS, sq=8, causal=True, window=700),
+                                               dict(chunk_tokens=480)),
     "bf16_mha_g1": (dict(seq_lens=LENS, num_heads=8, num_kv_heads=8), dict(chunk_tokens=48)),
     "bf16_g2_sq1": (dict(seq_lens=LENS, num_heads=4, num_kv_heads=2), dict()),
     "bf16_g8": (dict(seq_lens=LENS, num_heads=64, num_kv_heads=8), dict(chunk_tokens=96)),
