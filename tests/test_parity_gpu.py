@@ -340,6 +340,54 @@ def test_fp8_long_b8_full(variant):
         _check_full(case, ref, **VARIANTS[variant])
 
 
+@pytest.mark.parametrize("hkv,window", [(1, 0), (2, 0), (2, 70000)])
+def test_tcgen05_units_over_many_ctas(hkv, window):
+    """One 300,000-key request, 32 query heads per kv head (M = 32).  With one
+    kv head its 147 chunks each get a CTA (147 pieces); with two, CTAs take tile
+    shares of about 31 tiles, so each unit is cut into about 76 pieces.  Either
+    way the CTA completing a unit's last piece merges its pieces in blocks of
+    32."""
+    import paged_kv_decode_15_gb300 as pkd
+    case = wl.paged_case(name="long_units", seq_lens=[300_000], sq=1, num_heads=32 * hkv, num_kv_heads=hkv,
+                         seed=91, window=window)
+    assert pkd.kernel_name(1, 1, 32 * hkv, hkv, 128, 16, 300_000, pkd.BF16, window=window) == \
+        "persistent tcgen05 kernel, TMEM accumulators"
+    _check(case)
+
+
+def _check_fp32_then_rounding(case, what):
+    """Short requests put many outputs near |4|, where half a bf16 ulp alone is
+    0.0078: the arithmetic is compared on the fp32 output (at the bf16
+    tolerance) and the 16-bit output is checked to be that fp32 output rounded
+    to nearest even, bit for bit."""
+    import paged_kv_decode_15_gb300 as pkd
+    ref, rlse = gu.oracle_paged(case)
+    q = gu.to_dev(case.q, case.dtype)
+    cache = gu.to_dev(case.kv_cache, case.dtype)
+    bt = gu.to_dev(case.block_table, "int32")
+    dl = gu.to_dev(case.seq_lens, "int32")
+    kw = dict(q_scale=case.q_scale, k_scale=case.k_scale, v_scale=case.v_scale)
+    o32, lse = pkd.paged_decode(q, cache, bt, dl, case.scale, case.window, out_dtype=torch.float32, **kw)
+    o16, lse16 = pkd.paged_decode(q, cache, bt, dl, case.scale, case.window, out_dtype=torch.bfloat16, **kw)
+    torch.cuda.synchronize()
+    tol = gu.TOL_OUT_FP8 if case.dtype == "fp8" else gu.TOL_OUT
+    gu.assert_close(o32.double().cpu().numpy(), ref, tol, f"{what} out (fp32)")
+    gu.assert_close(lse.double().cpu().numpy(), rlse, gu.TOL_LSE, f"{what} lse")
+    assert torch.equal(o16.cpu().view(torch.int16), o32.cpu().to(torch.bfloat16).view(torch.int16))
+    assert torch.equal(lse16.cpu(), lse.cpu())
+
+
+def test_tcgen05_largest_batch():
+    """512 requests (the tcgen05 kernel's batch limit) of 0-300 keys, 32 rows
+    per kv head: more units than CTAs, many cut by shares, some empty."""
+    import paged_kv_decode_15_gb300 as pkd
+    lens = np.random.default_rng(93).integers(0, 301, size=512).astype(np.int32)
+    lens[::37] = 0
+    case = wl.paged_case(name="b512", seq_lens=lens, sq=8, seed=94)
+    assert pkd.kernel_name(512, 8, 32, 8, 128, 16, 300, pkd.BF16) == "persistent tcgen05 kernel, TMEM accumulators"
+    _check_fp32_then_rounding(case, "b512")
+
+
 @pytest.mark.parametrize("sq", [1, 8])
 def test_long_slices_reload_the_page_list(sq):
     """One 2M-key request on the per-CTA partition: every CTA streams more keys
@@ -352,24 +400,7 @@ def test_long_slices_reload_the_page_list(sq):
 @pytest.mark.parametrize("dtype,sq", [("fp8", 1), ("bf16", 8)])
 def test_batch_above_the_flat_table_limit(dtype, sq):
     """1500 short requests (0-69 keys): the chunked grid (e4m3 warp, or warp
-    pairs for 32 rows).  With so few keys many outputs lie near |4|, where half
-    a bf16 ulp alone is 0.0078, so the arithmetic is compared on the fp32
-    output (at the bf16 tolerance) and the 16-bit output is checked to be that
-    fp32 output rounded to nearest even, bit for bit."""
-    import paged_kv_decode_15_gb300 as pkd
+    pairs for 32 rows)."""
     lens = np.random.default_rng(77).integers(0, 70, size=1500).astype(np.int32)
     case = wl.paged_case(name="wide", seq_lens=lens, sq=sq, dtype=dtype, seed=78)
-    ref, rlse = gu.oracle_paged(case)
-    q = gu.to_dev(case.q, dtype)
-    cache = gu.to_dev(case.kv_cache, dtype)
-    bt = gu.to_dev(case.block_table, "int32")
-    dl = gu.to_dev(case.seq_lens, "int32")
-    kw = dict(q_scale=case.q_scale, k_scale=case.k_scale, v_scale=case.v_scale)
-    o32, lse = pkd.paged_decode(q, cache, bt, dl, case.scale, 0, out_dtype=torch.float32, **kw)
-    o16, lse16 = pkd.paged_decode(q, cache, bt, dl, case.scale, 0, out_dtype=torch.bfloat16, **kw)
-    torch.cuda.synchronize()
-    tol = gu.TOL_OUT_FP8 if dtype == "fp8" else gu.TOL_OUT
-    gu.assert_close(o32.double().cpu().numpy(), ref, tol, "wide out (fp32)")
-    gu.assert_close(lse.double().cpu().numpy(), rlse, gu.TOL_LSE, "wide lse")
-    assert torch.equal(o16.cpu().view(torch.int16), o32.cpu().to(torch.bfloat16).view(torch.int16))
-    assert torch.equal(lse16.cpu(), lse.cpu())
+    _check_fp32_then_rounding(case, "wide")
