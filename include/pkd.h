@@ -199,8 +199,8 @@ pkd_status pkd_paged_decode(const void* q, pkd_dtype q_dtype,
  * scratch array: calls that may overlap on the GPU (different streams, or
  * different host threads on one device) race and must be serialised by the
  * caller.  The device-side status word (out-of-range lengths or pages, a
- * wait that timed out) is cleared by the next call and never reported:
- * callers that need it use pkd_paged_decode with their own workspace.
+ * wait that timed out) is cleared by the next call: read it with
+ * pkd_paged_decode_static_check before then.
  */
 pkd_status pkd_paged_decode_static(const void* q, pkd_dtype q_dtype,
                                    const void* kv_cache, pkd_dtype kv_dtype, int64_t num_pages,
@@ -211,6 +211,17 @@ pkd_status pkd_paged_decode_static(const void* q, pkd_dtype q_dtype,
                                    float scale, float q_scale, float k_scale, float v_scale, int window,
                                    void* out, pkd_dtype out_dtype, float* lse,
                                    int chunk_tokens, unsigned flags, void* stream);
+
+/*
+ * The device-side status word of the last pkd_paged_decode_static call on
+ * the current device, like pkd_workspace_check on a caller workspace: waits
+ * for `stream`, returns PKD_OK, PKD_EDEVICE_BOUNDS (a seq_lens entry outside
+ * [0, max_kv_len] or a block-table entry outside [0, num_pages): those keys
+ * were skipped) or PKD_ETIMEOUT (a kernel gave up waiting on its own copies),
+ * and clears the word.  No counterpart in the pages (see
+ * pkd_paged_decode_static).  Allocates nothing.
+ */
+pkd_status pkd_paged_decode_static_check(void* stream);
 
 /*
  * KV-cache write [TS FlashInferTSImpl.do_kv_cache_update, reshape_and_cache_flash]:

@@ -27,7 +27,8 @@ FLAG_TEST_TIMEOUT = 64
 
 SYMBOLS = ("pkd_version", "pkd_last_error", "pkd_paged_decode_workspace_size", "pkd_paged_decode_kernel_name",
            "pkd_workspace_init",
-           "pkd_workspace_check", "pkd_paged_decode", "pkd_paged_decode_static", "pkd_cache_write",
+           "pkd_workspace_check", "pkd_paged_decode", "pkd_paged_decode_static", "pkd_paged_decode_static_check",
+           "pkd_cache_write",
            "pkd_segmented_attention", "pkd_segmented_attention_paged", "pkd_lse_merge")
 
 
@@ -69,13 +70,14 @@ def load_library(path: str = LIB_PATH):
                                      P, I, P, P, SZ, I, U, P]
     lib.pkd_paged_decode_static.argtypes = [P, I, P, I, I64, P, I64, P, I, I, I, I, I, I, I, F, F, F, F, I,
                                             P, I, P, I, U, P]
+    lib.pkd_paged_decode_static_check.argtypes = [P]
     lib.pkd_cache_write.argtypes = [P, P, I, I64, I64, P, I64, I, I, I, I64, P, I, F, F, P]
     lib.pkd_segmented_attention.argtypes = [P, P, P, I, P, P, I, I, I, I, I, I, I, P, P, P, P]
     lib.pkd_segmented_attention_paged.argtypes = [P, I, P, I64, P, I64, P, P, P, I, I, I, I, I, I, I, I, I,
                                                   P, P, P, P]
     lib.pkd_lse_merge.argtypes = [P, P, P, P, I, I, I, I, P, I, P, P]
     for name in ("pkd_workspace_init", "pkd_workspace_check", "pkd_paged_decode", "pkd_paged_decode_static",
-                 "pkd_cache_write", "pkd_segmented_attention", "pkd_segmented_attention_paged", "pkd_lse_merge"):
+                 "pkd_paged_decode_static_check", "pkd_cache_write", "pkd_segmented_attention", "pkd_segmented_attention_paged", "pkd_lse_merge"):
         getattr(lib, name).restype = I
     _lib = lib
     return lib

@@ -81,3 +81,12 @@ extern "C" pkd_status pkd_paged_decode_static(const void* q, pkd_dtype q_dtype, 
                             k_scale, v_scale, window, out, out_dtype, lse, scratch, kStaticScratchBytes,
                             chunk_tokens, flags, stream);
 }
+
+extern "C" pkd_status pkd_paged_decode_static_check(void* stream) {
+    void* scratch = nullptr;
+    const cudaError_t e = scratch_address(&scratch);
+    if (e != cudaSuccess)
+        return pkd::report(PKD_ECUDA, "static scratch address: %s", cudaGetErrorString(e));
+    // the status word sits at the start of the scratch, as in a caller workspace
+    return pkd_workspace_check(scratch, kStaticScratchBytes, stream);
+}

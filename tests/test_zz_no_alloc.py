@@ -84,3 +84,23 @@ def test_static_scratch_rejects_plans_above_its_size():
                                      2048, 0.1, 1.0, 1.0, 1.0, 0, None, pkd.BF16, None, 16, 0, None)
     assert st == pkd.EUNSUPPORTED
     assert b"static" in lib.pkd_last_error()
+
+
+def test_static_check_reports_and_clears_the_status_word():
+    """The static call's status word is read back by its companion check: a
+    length above max_kv_len is clamped and reported, then the word is clear."""
+    import paged_kv_decode_15_gb300 as pkd
+    lib = pkd.load_library()
+    case = wl.paged_case(name="static_bad", seq_lens=[100, 50], seed=9, table_width=8)
+    d = dict(q=gu.to_dev(case.q, "bf16"), cache=gu.to_dev(case.kv_cache, "bf16"),
+             bt=gu.to_dev(case.block_table, "int32"), lens=gu.to_dev(case.seq_lens, "int32"), max_kv_len=128)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    out = torch.empty(case.q.shape, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(case.q.shape[:3], dtype=torch.float32, device="cuda")
+    assert lib.pkd_paged_decode_static(*_args(case, d, out, lse, pkd.BF16), 0, 0, stream) == pkd.OK
+    assert lib.pkd_paged_decode_static_check(stream) == pkd.OK
+    d["lens"][0] = 500  # above max_kv_len: clamped and reported
+    assert lib.pkd_paged_decode_static(*_args(case, d, out, lse, pkd.BF16), 0, 0, stream) == pkd.OK
+    assert lib.pkd_paged_decode_static_check(stream) == pkd.EDEVICE_BOUNDS
+    assert lib.pkd_paged_decode_static_check(stream) == pkd.OK  # the word was cleared
+    assert torch.isfinite(out.float()).all()
