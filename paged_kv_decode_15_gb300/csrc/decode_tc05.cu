@@ -4,10 +4,10 @@
 
 namespace pkd {
 
-template <bool kBF16>
+template <bool kBF16, bool kCausal>
 static cudaError_t launch_tc(const CUtensorMap& kvmap, const CUtensorMap& qmap, const DecodeParams& p,
                              cudaStream_t stream) {
-    auto kern = decode_tc05_kernel<kBF16>;
+    auto kern = decode_tc05_kernel<kBF16, kCausal>;
     static PerDevice state;
     int per_sm = 1, grid = 1;
     cudaError_t e = kernel_setup(state, kern, kTcThreads, TcShape::SMEM, &per_sm);
@@ -20,7 +20,9 @@ static cudaError_t launch_tc(const CUtensorMap& kvmap, const CUtensorMap& qmap, 
 
 cudaError_t launch_decode_tc05(bool bf16, const CUtensorMap& kvmap, const CUtensorMap& qmap, const DecodeParams& p,
                                cudaStream_t stream) {
-    return bf16 ? launch_tc<true>(kvmap, qmap, p, stream) : launch_tc<false>(kvmap, qmap, p, stream);
+    if (p.causal)
+        return bf16 ? launch_tc<true, true>(kvmap, qmap, p, stream) : launch_tc<false, true>(kvmap, qmap, p, stream);
+    return bf16 ? launch_tc<true, false>(kvmap, qmap, p, stream) : launch_tc<false, false>(kvmap, qmap, p, stream);
 }
 
 }  // namespace pkd

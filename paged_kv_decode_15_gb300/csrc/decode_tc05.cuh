@@ -291,7 +291,7 @@ __device__ __forceinline__ void tc_merge_unit(const DecodeParams& p, long long u
     }
 }
 
-template <bool kBF16>
+template <bool kBF16, bool kCausal>
 __global__ void __launch_bounds__(kTcThreads, 1)
 decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_constant__ CUtensorMap qmap,
                    const DecodeParams p) {
@@ -688,7 +688,7 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
                 bool valid = key < nvalid;
                 // causal: this key is visible to the rows [rmin, rmax) of the group
                 int rmin = 0, rmax = RG;
-                if (p.causal) {
+                if constexpr (kCausal) {
                     const int d = tok0 + key - first_pos;  // first token that sees the key
                     rmin = d * p.G - rbase;
                     if (p.window > 0) rmax = (d + p.window) * p.G - rbase;
@@ -705,8 +705,9 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
                     mbar_arrive(bar(S::B_SE + sbuf));
 #pragma unroll
                     for (int r = 0; r < RG; ++r)
-                        x[r] = (valid && rbase + r < M && r >= rmin && r < rmax) ? __uint_as_float(sr[r]) * scale2
-                                                                                  : -INFINITY;
+                        x[r] = (valid && rbase + r < M && (!kCausal || (r >= rmin && r < rmax)))
+                                   ? __uint_as_float(sr[r]) * scale2
+                                   : -INFINITY;
                 } else {
 #pragma unroll
                     for (int r = 0; r < RG; ++r) x[r] = -INFINITY;
