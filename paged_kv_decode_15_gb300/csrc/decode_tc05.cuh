@@ -17,9 +17,9 @@
 // cuts it.  Per 128-key tile of an item:
 //   S^T = K Q^T      tcgen05.mma, M = 128 keys, N = 32 query rows, K = 128
 //                    dims: A = the K tile as TMA lands it (K-major, 128-byte
-//                    swizzle), B = the item's q rows (K-major); S^T in TMEM.
+//                    swizzle), B = the run's q rows (K-major); S^T in TMEM.
 //   softmax          one key per thread of a warp group (TMEM lane = key):
-//                    tcgen05.ld of its 32 scores, online softmax per query
+//                    tcgen05.ld of its group's 16 scores, online softmax per query
 //                    row in fp32 whose reference maximum moves only when a
 //                    row's maximum grows by more than 2^8 (then O and l are
 //                    rescaled), P written in the operand type over the
