@@ -273,14 +273,12 @@ pkd_status get_map(CUtensorMap& out, const void* base, int rank, uint64_t d0, ui
 
 // The "stage map" of a paged cache: {128-byte chunk, key row, chunk of the
 // row}, strides {row bytes, 128 B}, box {one chunk, 16 rows, every chunk},
-// so one TMA copy loads a 16-key stage (K and V) chunk-major.  With
-// half_rows the box is {one chunk, 8 rows, one chunk}: one copy per chunk
-// fills the first 8 rows of that chunk's 16-row slot.
-// Boxes of the stage map: a whole 16-key stage (every chunk), its first 8
-// rows of one chunk, or the tcgen05 kernel's stage: a 4-D view {chunk
-// elements, 8 rows, chunk, 8-row group} whose box {all, 8, all, 2} lands a
-// 16-key stage as two 8-row groups, each holding every chunk of its rows.
-enum StageBox { kStageFull = 0, kStageHalfRows = 1, kStageTcGroup = 2 };
+// so one TMA copy loads a 16-key stage (K and V) chunk-major.
+// Boxes of the stage map: a whole 16-key stage (every chunk), or the tcgen05
+// kernel's stage: a 4-D view {chunk elements, 8 rows, chunk, 8-row group}
+// whose box {all, 8, all, 2} lands a 16-key stage as two 8-row groups, each
+// holding every chunk of its rows.
+enum StageBox { kStageFull = 0, kStageTcGroup = 2 };
 
 pkd_status get_stage_map(CUtensorMap& out, const void* cache, uint64_t rows, int row_bytes, pkd_dtype dt,
                          StageBox mode = kStageFull) {
@@ -288,7 +286,7 @@ pkd_status get_stage_map(CUtensorMap& out, const void* cache, uint64_t rows, int
     MapKey k;
     std::memset(&k, 0, sizeof k);
     k.base = cache; k.d0 = 128 / elt; k.d1 = rows; k.d2 = row_bytes / 128; k.s1 = row_bytes; k.s2 = 128;
-    k.rank = mode == kStageHalfRows ? 108 : mode == kStageTcGroup ? 140 : 103; k.dtype = dt;
+    k.rank = mode == kStageTcGroup ? 140 : 103; k.dtype = dt;
     MapCache& c = map_cache();
     {
         std::lock_guard<std::mutex> g(c.mu);
@@ -316,8 +314,7 @@ pkd_status get_stage_map(CUtensorMap& out, const void* cache, uint64_t rows, int
     } else {
         cuuint64_t dims[3] = {k.d0, k.d1, k.d2};
         cuuint64_t strides[2] = {k.s1, k.s2};
-        cuuint32_t box[3] = {(cuuint32_t)(128 / elt), (cuuint32_t)(mode == kStageFull ? pkd::kStageTok : pkd::kStageTok / 2),
-                             (cuuint32_t)(mode == kStageHalfRows ? 1 : row_bytes / 128)};
+        cuuint32_t box[3] = {(cuuint32_t)(128 / elt), (cuuint32_t)pkd::kStageTok, (cuuint32_t)(row_bytes / 128)};
         cuuint32_t estr[3] = {1, 1, 1};
         r = enc(&m, t, 3, const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -657,8 +654,8 @@ pkd_status pkd_segmented_attention_paged(const void* q, pkd_dtype dtype, const v
     const uint64_t rows = (uint64_t)num_pages * num_kv_heads * page_size;
     pkd_status st = get_stage_map(p.kmap, kv_cache, rows, 4 * head_dim, dtype);
     if (st != PKD_OK) return st;
-    st = get_stage_map(p.vmap, kv_cache, rows, 4 * head_dim, dtype, kStageHalfRows);  // stages whose keys end in 8 rows
-    if (st != PKD_OK) return st;
+    p.vmap = p.kmap;  // unused: a stage's K and V rows come in one copy
+    p.cache = kv_cache;
     p.paged = 1;
     page_magic(page_size, p.pmagic, p.pmshift);
     p.block_table = block_table;

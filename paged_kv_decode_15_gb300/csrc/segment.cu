@@ -44,6 +44,21 @@ __device__ __forceinline__ int seg_page_col(const SegmentParams& p, int tok) {
     return page_div(tok, p.pmagic, p.pmshift);
 }
 
+// One 16-byte copy into shared memory that completes asynchronously; with
+// `nbytes` = 0 it reads nothing and writes 16 zero bytes.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, int nbytes, uint64_t policy) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(dst), "l"(src), "r"(nbytes),
+                 "l"(policy)
+                 : "memory");
+}
+
+// An arrive on `bar` once this thread's earlier cp.async copies have landed;
+// it raises the barrier's pending count first, so the phase still waits for
+// its ordinary arrivals as well.
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
     for (int m = 16; m >= 1; m >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, m));
@@ -189,6 +204,11 @@ segmented_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     const uint32_t ring = smem_u32(ring_gen);
     const uint32_t bar0 = smem_u32(bars + warp * kSegNbuf);
     const uint64_t pol = policy_evict_first();
+    // Called by all 32 lanes: a full stage is one TMA copy issued by lane 0; a
+    // paged stage that the segment covers only in part is copied row-exactly,
+    // 16 bytes a lane, into the layout the 128-byte-swizzled copies give
+    // (16-byte piece j of row r at ((j ^ (r & 7)) << 4) in its 128-byte chunk),
+    // rows outside the segment zero-filled without being read.
     auto issue = [&](int k) {
         int g, sidx;
         stage_of(issue_cur, k, g, sidx);
@@ -197,23 +217,34 @@ segmented_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         if constexpr (kPaged) {
             const int pg = spage[pre[g] + sidx];
             if (pg < 0) {
-                mbar_arrive(bar);
+                if (lane == 0) mbar_arrive(bar);
                 return;
             }
             const int tok0 = sa[g] + sidx * kStageTok;
             const int crow = (pg * p.Hkv + hk) * p.P + (tok0 - seg_page_col(p, tok0) * p.P);
-            if (ss[g] + su[g] - tok0 <= kStageTok / 2) {
-                // the segment ends in the stage's first 8 rows: load only those
-                // (rows 8..15 are masked and their V rows zeroed before use)
-                mbar_arrive_expect_tx(bar, S::STAGE / 2);
-#pragma unroll
-                for (int c = 0; c < D * 4 / 128; ++c) tma_load_3d(buf + c * 2048, &vmap, 0, crow, c, bar, pol);
+            const int r0 = max(0, ss[g] - tok0), r1 = min(kStageTok, ss[g] + su[g] - tok0);
+            if (r0 > 0 || r1 < kStageTok) {
+                constexpr int ROWB = D * 4, PIECES = ROWB / 16;  // a cache row: K then V, bf16/fp16
+                const uint8_t* src = static_cast<const uint8_t*>(p.cache) + static_cast<long long>(crow) * ROWB;
+#pragma unroll 4
+                for (int e = lane; e < kStageTok * PIECES; e += 32) {
+                    const int row = e / PIECES, pc = e % PIECES, j = pc & 7;
+                    const bool in = row >= r0 && row < r1;
+                    cp_async_16(buf + (pc >> 3) * 2048 + row * 128 + ((j ^ (row & 7)) << 4),
+                                src + (in ? row : r0) * ROWB + pc * 16, in ? 16 : 0, pol);
+                }
+                cp_async_mbar_arrive(bar);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar);
                 return;
             }
-            mbar_arrive_expect_tx(bar, S::STAGE);
-            tma_load_3d(buf, &kmap, 0, crow, 0, bar, pol);
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar, S::STAGE);
+                tma_load_3d(buf, &kmap, 0, crow, 0, bar, pol);
+            }
             return;
         }
+        if (lane != 0) return;
         const long long row = row_base + (g < p.topk ? static_cast<long long>(g) * p.bs : static_cast<long long>(p.topk) * p.bs) +
                               stage_row(g, sidx);
         mbar_arrive_expect_tx(bar, S::STAGE);
@@ -258,8 +289,7 @@ segmented_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         }
         __syncwarp();
     }
-    if (lane == 0)
-        for (int k = 0; k < kSegNbuf && k < my_n; ++k) issue(k);
+    for (int k = 0; k < kSegNbuf && k < my_n; ++k) issue(k);
 
     MmaWarp<D, kBF16, 1, NT> wp;
     wp.load_q(smem_u32(qs), S::QSTRIDE, lane);
@@ -317,11 +347,13 @@ segmented_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             nvalid = min(kStageTok, su[g] - sidx * kStageTok);
         }
         const uint32_t st = ring + buf * S::STAGE;
-        if (nvalid < kStageTok) zero_tail_v<D, 2>(ring_gen + buf * S::STAGE, nvalid, lane);
+        // rows past the segment hold stale values unless a partial paged stage
+        // zero-filled them: P.V must not meet them (masked keys weigh 0, 0 * NaN is not 0)
+        if (nvalid < kStageTok && (!kPaged || nvalid == 0)) zero_tail_v<D, 2>(ring_gen + buf * S::STAGE, nvalid, lane);
         wp.consume(st, S::HALF, nvalid, nvalid < kStageTok || lo > 0, p.scale_log2, kSegOut ? 0.f : sb[g],
                    [&](int row, int kt) { return row < M && kt >= lo; }, lane);
         __syncwarp();
-        if (lane == 0 && k + kSegNbuf < my_n) {
+        if (k + kSegNbuf < my_n) {
             fence_proxy_async();
             issue(k + kSegNbuf);
         }

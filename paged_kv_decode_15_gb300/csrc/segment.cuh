@@ -9,9 +9,10 @@ namespace pkd {
 struct SegmentParams {
     CUtensorMap kmap, vmap;   // 3-D maps over k, v: {head_dim, Hkv, rows}; paged: kmap is the
                               // cache's stage map {128-byte chunk, pages*Hkv*P rows, chunks}
-                              // and vmap the same map with 8-row, one-chunk boxes
+                              // and vmap is unused
     const int32_t* block_table;  // paged: [n, bt_stride]
     const int32_t* seg_start;    // paged: [n, topk+1] first key position of each segment
+    const void* cache;           // paged: the cache itself, for row-exact copies of partial stages
     long long bt_stride, num_pages;
     int P, max_kv_len, paged;
     uint32_t pmagic;          // paged: tok / P == (tok * pmagic) >> pmshift for 0 <= tok < 2^31
