@@ -596,6 +596,8 @@ pkd_status pkd_segmented_attention(const void* q, const void* k, const void* v, 
     std::memset(&p, 0, sizeof p);
     p.kmap = kmap;
     p.vmap = vmap;
+    p.k = k;
+    p.v = v;
     p.q = q;
     p.used = used;
     p.bias = bias;
@@ -655,7 +657,7 @@ pkd_status pkd_segmented_attention_paged(const void* q, pkd_dtype dtype, const v
     pkd_status st = get_stage_map(p.kmap, kv_cache, rows, 4 * head_dim, dtype);
     if (st != PKD_OK) return st;
     p.vmap = p.kmap;  // unused: a stage's K and V rows come in one copy
-    p.cache = kv_cache;
+    p.k = kv_cache;
     p.paged = 1;
     page_magic(page_size, p.pmagic, p.pmshift);
     p.block_table = block_table;

@@ -193,7 +193,7 @@ segmented_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     // whose length is not a multiple of 16 is moved back to end at the
     // segment's last used row; its first rows (read again, from L2) are masked
     // as already consumed.  No row past the used prefix is then read from
-    // DRAM.  A segment shorter than a stage reads one stage from its start.
+    // DRAM.  A segment shorter than a stage copies its used rows only.
     auto shifted = [&](int g, int sidx) {
         const int u = su[g];
         return !kPaged && u > kStageTok && (u % kStageTok) != 0 && sidx == (u - 1) / kStageTok;
@@ -204,11 +204,33 @@ segmented_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     const uint32_t ring = smem_u32(ring_gen);
     const uint32_t bar0 = smem_u32(bars + warp * kSegNbuf);
     const uint64_t pol = policy_evict_first();
-    // Called by all 32 lanes: a full stage is one TMA copy issued by lane 0; a
-    // paged stage that the segment covers only in part is copied row-exactly,
-    // 16 bytes a lane, into the layout the 128-byte-swizzled copies give
-    // (16-byte piece j of row r at ((j ^ (r & 7)) << 4) in its 128-byte chunk),
-    // rows outside the segment zero-filled without being read.
+    // Rows [r0, r1) of a stage copied row-exactly by the warp's 32 lanes, 16
+    // bytes a lane, into the layout the 128-byte-swizzled copies give (16-byte
+    // piece j of row r at ((j ^ (r & 7)) << 4) in its 128-byte chunk, the K
+    // chunks then the V chunks); the other rows are zero-filled without a read.
+    // The lanes' copies signal the stage's barrier on landing, lane 0 arrives.
+    auto copy_rows = [&](uint32_t buf, uint32_t bar, const uint8_t* kb, const uint8_t* vb, long long rstride, int r0,
+                         int r1) {
+        constexpr int HP = D * 2 / 16;  // 16-byte pieces of a K (or V) row
+        constexpr int PR = 2 * HP;      // of a stage row, K then V
+        constexpr int RPP = 32 / PR;    // rows per pass of the warp
+        const int pc = lane % PR, j = pc & 7;
+        const uint8_t* src = (pc < HP ? kb : vb) + (pc % HP) * 16;
+        const uint32_t dst = buf + (pc >> 3) * 2048;
+#pragma unroll
+        for (int it = 0; it < kStageTok / RPP; ++it) {
+            const int row = it * RPP + lane / PR;
+            const bool in = row >= r0 && row < r1;
+            cp_async_16(dst + row * 128 + ((j ^ (row & 7)) << 4), src + (in ? row : r0) * rstride, in ? 16 : 0, pol);
+        }
+        cp_async_mbar_arrive(bar);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar);
+    };
+    // Called by all 32 lanes.  A stage the segment covers whole is one TMA copy
+    // (two per half in the contiguous mode) issued by lane 0; a stage it covers
+    // in part is copied row-exactly: in the paged mode a segment's first or
+    // last stage, in the contiguous mode a segment shorter than a stage.
     auto issue = [&](int k) {
         int g, sidx;
         stage_of(issue_cur, k, g, sidx);
@@ -224,18 +246,8 @@ segmented_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             const int crow = (pg * p.Hkv + hk) * p.P + (tok0 - seg_page_col(p, tok0) * p.P);
             const int r0 = max(0, ss[g] - tok0), r1 = min(kStageTok, ss[g] + su[g] - tok0);
             if (r0 > 0 || r1 < kStageTok) {
-                constexpr int ROWB = D * 4, PIECES = ROWB / 16;  // a cache row: K then V, bf16/fp16
-                const uint8_t* src = static_cast<const uint8_t*>(p.cache) + static_cast<long long>(crow) * ROWB;
-#pragma unroll 4
-                for (int e = lane; e < kStageTok * PIECES; e += 32) {
-                    const int row = e / PIECES, pc = e % PIECES, j = pc & 7;
-                    const bool in = row >= r0 && row < r1;
-                    cp_async_16(buf + (pc >> 3) * 2048 + row * 128 + ((j ^ (row & 7)) << 4),
-                                src + (in ? row : r0) * ROWB + pc * 16, in ? 16 : 0, pol);
-                }
-                cp_async_mbar_arrive(bar);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar);
+                const uint8_t* kb = static_cast<const uint8_t*>(p.k) + static_cast<long long>(crow) * (D * 4);
+                copy_rows(buf, bar, kb, kb + D * 2, D * 4, r0, r1);  // a cache row: K then V
                 return;
             }
             if (lane == 0) {
@@ -244,9 +256,15 @@ segmented_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             }
             return;
         }
-        if (lane != 0) return;
         const long long row = row_base + (g < p.topk ? static_cast<long long>(g) * p.bs : static_cast<long long>(p.topk) * p.bs) +
                               stage_row(g, sidx);
+        if (su[g] < kStageTok) {
+            const long long off = (row * p.Hkv + hk) * (D * 2);
+            copy_rows(buf, bar, static_cast<const uint8_t*>(p.k) + off, static_cast<const uint8_t*>(p.v) + off,
+                      static_cast<long long>(p.Hkv) * D * 2, 0, su[g]);
+            return;
+        }
+        if (lane != 0) return;
         mbar_arrive_expect_tx(bar, S::STAGE);
 #pragma unroll
         for (int bx = 0; bx < D * 2 / 128; ++bx) {
@@ -347,9 +365,10 @@ segmented_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             nvalid = min(kStageTok, su[g] - sidx * kStageTok);
         }
         const uint32_t st = ring + buf * S::STAGE;
-        // rows past the segment hold stale values unless a partial paged stage
-        // zero-filled them: P.V must not meet them (masked keys weigh 0, 0 * NaN is not 0)
-        if (nvalid < kStageTok && (!kPaged || nvalid == 0)) zero_tail_v<D, 2>(ring_gen + buf * S::STAGE, nvalid, lane);
+        // a stage of a missing page holds stale values: P.V must not meet them
+        // (masked keys weigh 0, and 0 * NaN is not 0); a partial stage's rows
+        // outside the segment were zero-filled by its copies
+        if (nvalid == 0) zero_tail_v<D, 2>(ring_gen + buf * S::STAGE, 0, lane);
         wp.consume(st, S::HALF, nvalid, nvalid < kStageTok || lo > 0, p.scale_log2, kSegOut ? 0.f : sb[g],
                    [&](int row, int kt) { return row < M && kt >= lo; }, lane);
         __syncwarp();

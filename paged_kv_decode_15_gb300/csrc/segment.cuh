@@ -12,7 +12,8 @@ struct SegmentParams {
                               // and vmap is unused
     const int32_t* block_table;  // paged: [n, bt_stride]
     const int32_t* seg_start;    // paged: [n, topk+1] first key position of each segment
-    const void* cache;           // paged: the cache itself, for row-exact copies of partial stages
+    const void* k;               // k rows [rows, Hkv, D] (paged: the cache), for row-exact copies
+    const void* v;               // v rows [rows, Hkv, D] (paged: unused)
     long long bt_stride, num_pages;
     int P, max_kv_len, paged;
     uint32_t pmagic;          // paged: tok / P == (tok * pmagic) >> pmshift for 0 <= tok < 2^31
