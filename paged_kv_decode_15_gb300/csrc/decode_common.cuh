@@ -281,18 +281,19 @@ __device__ void cta_finish_parts(const DecodeParams& p, const CtaWork& w, const 
     }
     if (single) return;
 
-    // Split-KV: the last CTA of (b, hk) to arrive merges every chunk.
-    __threadfence();
+    // Split-KV: the last CTA of (b, hk) to arrive merges every chunk.  The
+    // CTA barrier orders every thread's partial stores before one arrival with
+    // acquire-release semantics at GPU scope (release covers them; the acquire,
+    // passed on by the next barrier, covers the other chunks' partials).
     __syncthreads();
     if (threadIdx.x == 0) {
-        const int prev = atomicAdd(p.counters + unit, 1);
+        const int prev = atom_add_acq_rel_gpu(p.counters + unit);
         const int last = prev == w.nsplit - 1;
         if (last) atomicExch(p.counters + unit, 0);  // ready for the next call
         *flag = last;
     }
     __syncthreads();
     if (!*flag) return;
-    __threadfence();
     for (int e = threadIdx.x; e < M * D; e += blockDim.x) {
         const int r = e / D, d = e % D;
         float mx = -INFINITY;

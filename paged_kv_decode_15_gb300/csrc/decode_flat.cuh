@@ -265,18 +265,19 @@ decode_flat_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams 
         float* sl = p.part_lse + (wid * 2 + side) * p.M;
         wp.emit([&](int r, int d, float v) { r += row0; if (r < p.M) __stcg(so + r * D + d, v); }, lane);
         wp.emit_lse([&](int r, float l2) { r += row0; if (r < p.M) __stcg(sl + r, l2); }, lane);
-        __threadfence();
+        // the warp's stores, then one arrival with acquire-release semantics at
+        // GPU scope; the warp barrier after it passes the acquire on to every lane
         __syncwarp();
         const int u = b * p.Hkv + hk;
         int last = 0;
         if (lane == 0) {
-            const int prev = atomicAdd(p.counters + u, 1);
+            const int prev = atom_add_acq_rel_gpu(p.counters + u);
             last = prev == static_cast<int>((wl - wf + 1) * RT - 1);
             if (last) atomicExch(p.counters + u, 0);  // ready for the next call
         }
         last = __shfl_sync(kFull, last, 0);
         if (!last) return;
-        __threadfence();
+        __syncwarp();
         merge_unit<D>(p, b, hk, wf, wl, Stot, Weff, E, mstat, lane);
         __syncwarp();
     };

@@ -216,14 +216,6 @@ __device__ __forceinline__ float tc_pick(const float (&v)[32], int r) {
     return x;
 }
 
-// One arrival on a unit's counter, returning the count before it: a fetch-add
-// with acquire and release semantics at GPU scope.
-__device__ __forceinline__ int tc_arrive_acq_rel(int* counter) {
-    int prev;
-    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(prev) : "l"(counter) : "memory");
-    return prev;
-}
-
 // LSE merge of the `np` pieces (partial results) of a split unit, run by the
 // epilogue warps of the CTA that completed its last piece.  Warp q4 takes
 // query rows q4, q4 + 4, ... (four at a time); lane j reads piece j's LSE
@@ -898,7 +890,7 @@ decode_tc05_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_const
                 // barrier ordered before it); the arrival that completes the unit
                 // acquires the other pieces' partials for the whole group
                 tc_group_sync(2);
-                if (q4 == 0 && lane == 0) votes[24] = tc_arrive_acq_rel(p.counters + unit);
+                if (q4 == 0 && lane == 0) votes[24] = atom_add_acq_rel_gpu(p.counters + unit);
                 tc_group_sync(2);
                 if (votes[24] == np - 1) {
                     tc_merge_unit(p, unit, row0, np, q4, lane);
