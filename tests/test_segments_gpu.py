@@ -166,3 +166,48 @@ def test_paged_segments_match_oracle(name):
 def test_dash_paged_n256_full():
     s = wl.dash_paged_n256()
     gu.assert_close(_run_paged(s), _oracle_paged(s), gu.TOL_OUT, "dash paged")
+
+
+def test_paged_segments_at_any_start_read_no_row_outside():
+    """Segments start at any key (a page's last key, inside one 16-key stage,
+    across a page boundary), and every cache row of a request that no segment
+    of its query covers holds NaN: a stage the segments cover in part must not
+    let those rows into the result (they are not copied, or are masked with
+    their V zeroed)."""
+    import dataclasses
+    s = wl.paged_segment_case(name="any_start", n=12, num_heads=8, num_kv_heads=2, topk=5, bs=40, local=24,
+                              seed=77, seq_range=(60, 300))
+    P, caps = s.page_size, [s.bs] * s.topk + [s.local]
+    rng = np.random.default_rng(5)
+    seg_start, used = s.seg_start.copy(), s.used.copy()
+    for i in range(s.n):
+        L = int(s.seq_lens[i])
+        for g in range(s.topk + 1):
+            st = int(rng.integers(0, L))
+            seg_start[i, g], used[i, g] = st, int(rng.integers(0, min(caps[g], L - st) + 1))
+    # query 0: one key at a page's last row, five keys inside one stage, ten
+    # keys across a page boundary, a full-capacity block, the local segment at
+    # an odd offset
+    for g, (st, u) in enumerate([(P - 1, 1), (3 + P, 5), (2 * P - 3, 10), (7, s.bs), (0, 0), (33, s.local)]):
+        seg_start[0, g], used[0, g] = st, u
+    assert int(s.seq_lens[0]) >= 33 + s.local
+    cache = s.kv_cache.copy()
+    owner = {}
+    for i in range(s.n):
+        L = int(s.seq_lens[i])
+        covered = np.zeros(L, bool)
+        for g in range(s.topk + 1):
+            covered[seg_start[i, g]:seg_start[i, g] + used[i, g]] = True
+        for t in np.flatnonzero(~covered):
+            pg = int(s.block_table[i, t // P])
+            assert owner.setdefault(pg, i) == i, "pages are not shared between requests"
+            cache[pg, :, t % P, :] = wl.BF16_NAN if s.dtype == "bf16" else wl.FP16_NAN
+    s = dataclasses.replace(s, kv_cache=cache, seg_start=seg_start, used=used)
+    out = _run_paged(s)
+    assert np.isfinite(out).all()
+    gu.assert_close(out, _oracle_paged(s), gu.TOL_OUT, "any start")
+    out2, so, sl = _run_paged(s, segments=True)
+    ro, rso, rsl = _oracle_paged(s, segments=True)
+    gu.assert_close(out2, ro, gu.TOL_OUT, "any start out")
+    gu.assert_close(so, rso, gu.TOL_OUT, "any start seg_out")
+    gu.assert_close(sl, rsl, gu.TOL_LSE, "any start seg_lse")
