@@ -213,6 +213,35 @@ class PagedRunner:
         self.inputs = [in_buf]    # copied in every end-to-end step
         self.outputs = [out_buf]  # copied back every end-to-end step
         self.acct = algorithmic_bytes(case)
+        self.flags, self.kv_code = flags, kv_code
+
+    def prepare_host(self):
+        """Pinned host q, table and lengths (and out, lse) for calls with
+        host_io: the kernels read and write them in place over the host link.
+        Returns (bytes read from the host, bytes written to it) per call."""
+        torch, c = __import__("torch"), self.case
+        pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu())
+        self.hq, self.hbt, self.hlens = pin(self.q), pin(self.bt), pin(self.lens)
+        self.hout = torch.empty(self.out.shape, dtype=self.out.dtype, pin_memory=True)
+        self.hlse = torch.empty(self.lse.shape, dtype=torch.float32, pin_memory=True)
+        self.ws_host = torch.empty(self.pkd.workspace_size(
+            c.batch, c.sq, c.num_heads, c.num_kv_heads, c.head_dim, c.page_size, self.max_kv_len, self.kv_code,
+            c.window, self.chunk, self.flags | self.pkd.FLAG_HOST_IO), dtype=torch.uint8, device="cuda")
+        self.pkd.workspace_init(self.ws_host)
+        nbytes = lambda ts: sum(t.numel() * t.element_size() for t in ts)
+        return nbytes([self.hq, self.hbt, self.hlens]), nbytes([self.hout, self.hlse])
+
+    def call_host(self):
+        c = self.case
+        self.pkd.paged_decode(self.hq, self.cache, self.hbt, self.hlens, c.scale, c.window, out=self.hout,
+                              lse=self.hlse, q_scale=c.q_scale, k_scale=c.k_scale, v_scale=c.v_scale,
+                              max_kv_len=self.max_kv_len, workspace=self.ws_host, causal=c.causal,
+                              chunk_tokens=self.chunk, force_fma=self.path == "fma", grid=self.grid, flat=self.flat,
+                              balanced=self.balanced, host_io=True)
+
+    def check_host(self):
+        if self.pkd.workspace_check(self.ws_host) != self.pkd.OK:
+            raise RuntimeError("device status word set: " + self.pkd.load_library().pkd_last_error().decode())
 
     def call(self):
         c = self.case
@@ -459,24 +488,46 @@ def run_gpu(args, rank, world, dist):
     host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in runner.outputs]
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = sum(t.numel() * t.element_size() for t in host_out)
-    es = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ee = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    torch.cuda.synchronize()
-    for i in range(args.steps):
-        flush.zero_()
-        es[i].record(stream)
+
+    def copy_step():
         for dev, host in zip(runner.inputs, host_in):
             dev.copy_(host, non_blocking=True)
         runner.call()
         for dev, host in zip(runner.outputs, host_out):
             host.copy_(dev, non_blocking=True)
-        ee[i].record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = float(sum(s.elapsed_time(e) for s, e in zip(es, ee)))
-    runner.check()
+
+    def timed(step):
+        es = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ee = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        for _ in range(args.warmup):
+            flush.zero_()
+            step()
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            flush.zero_()
+            es[i].record(stream)
+            step()
+            ee[i].record(stream)
+        torch.cuda.synchronize()
+        return float(sum(s.elapsed_time(e) for s, e in zip(es, ee)))
+
+    e2e_copy_ms = None
+    if hasattr(runner, "call_host"):
+        # the kernels read the step's inputs from pinned host memory and write its
+        # results there (PKD_FLAG_HOST_IO); the copy-in / copy-out step is timed too
+        e2e_copy_ms = timed(copy_step)
+        runner.check()
+        h2d, d2h = runner.prepare_host()
+        e2e_ms = timed(runner.call_host)
+        runner.check_host()
+    else:
+        e2e_ms = timed(copy_step)
+        runner.check()
+    args.e2e_copy_ms = e2e_copy_ms
 
     if dist:
-        total_ms, e2e_ms = max_over_ranks([total_ms, e2e_ms], dist, "cuda")
+        total_ms, e2e_ms, copy_ms = max_over_ranks([total_ms, e2e_ms, args.e2e_copy_ms or 0.0], dist, "cuda")
+        args.e2e_copy_ms = copy_ms if args.e2e_copy_ms is not None else None
     return case, runner, step_ms, total_ms, e2e_ms, h2d, d2h, clocks
 
 
@@ -691,8 +742,12 @@ def main():
             "e2e": {"value": round(job_throughput(acct["kv"], world, steps, e2e_ms), 2), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "us_per_call": round(e2e_ms / steps * 1e3, 2),
-                    "note": ("q, block_table, seq_lens in from pinned host memory (one packed copy), out and lse "
-                             "back (one packed copy), every step; the KV cache is resident device state")
+                    **({"copy_path_us_per_call": round(args.e2e_copy_ms / steps * 1e3, 2)}
+                       if getattr(args, "e2e_copy_ms", None) is not None else {}),
+                    "note": ("q, block_table, seq_lens read by the kernels from pinned host memory and out, lse "
+                             "written there, in place over the host link (PKD_FLAG_HOST_IO), every step; the KV "
+                             "cache is resident device state. copy_path_us_per_call: the same step with one packed "
+                             "copy in and one out around a device-memory call")
                     if isinstance(runner, PagedRunner) else
                             ("key, value, slot_mapping in from pinned host memory; the cache is resident "
                              "device state") if isinstance(runner, CacheWriteRunner) else

@@ -52,6 +52,16 @@ typedef enum {
 #define PKD_FLAG_GRID 8u        /* the chunked grid: one CTA per Split-KV chunk */
 #define PKD_FLAG_FLAT 16u       /* the persistent flat partition whatever the shapes (batch <= 1024) */
 #define PKD_FLAG_BALANCED 32u   /* the persistent per-CTA partition (16-bit caches, tensor cores) */
+/* q, block_table, seq_lens, out and lse are pinned host memory (cudaHostAlloc,
+ * cudaMallocHost or cudaHostRegister), which under unified addressing has the
+ * same address on the device: the kernels read and write it in place over the
+ * host link, with no copy before or after the launch.  kv_cache and the
+ * workspace stay device memory.  Each of those five pointers is checked with
+ * cudaPointerGetAttributes (host memory mapped at the same address, else
+ * PKD_EINVAL).  The tcgen05 kernel, whose q goes through a tensor-map copy,
+ * is not used with it: its shapes run on the chunked grid instead (the
+ * workspace size and kernel name follow the flag). */
+#define PKD_FLAG_HOST_IO 128u
 /* Diagnostic: every wait on a stage's copy tests its barrier once instead of
  * waiting up to 200 ms, so a call reports PKD_ETIMEOUT whenever a copy has not
  * landed by its first test.  The kernels still let every issued copy land
@@ -121,6 +131,8 @@ pkd_status pkd_workspace_check(void* workspace, size_t workspace_bytes, void* st
  *   lse          device fp32 [batch, sq, num_heads] natural-log LSE, or NULL
  *   workspace    device, >= pkd_paged_decode_workspace_size(...) bytes,
  *                zeroed once by pkd_workspace_init; 256-byte aligned.
+ * With PKD_FLAG_HOST_IO, q, block_table, seq_lens, out and lse are pinned
+ * host memory instead, read and written by the kernels in place.
  *
  * Query head h reads KV head h / (num_heads / num_kv_heads).  Logits are
  * (scale * q_scale * k_scale) * q.k and the output is scaled by v_scale

@@ -24,6 +24,7 @@ OK, EINVAL, EUNSUPPORTED, ECUDA, EDEVICE_BOUNDS, ETIMEOUT = range(6)
 BF16, FP16, FP8_E4M3, FP32 = 0, 1, 2, 3
 FLAG_CAUSAL, FLAG_MMA_SMALL_M, FLAG_FMA, FLAG_GRID, FLAG_FLAT, FLAG_BALANCED = 1, 2, 4, 8, 16, 32
 FLAG_TEST_TIMEOUT = 64
+FLAG_HOST_IO = 128
 
 SYMBOLS = ("pkd_version", "pkd_last_error", "pkd_paged_decode_workspace_size", "pkd_paged_decode_kernel_name",
            "pkd_workspace_init",
@@ -165,18 +166,27 @@ def _workspace(nbytes: int, device) -> torch.Tensor:
 def paged_decode(q, kv_cache, block_table, seq_lens, scale, window=0, out=None, lse=None, *, q_scale=1.0,
                  k_scale=1.0, v_scale=1.0, max_kv_len=None, workspace=None, chunk_tokens=0, causal=False,
                  mma_small_m=False, force_fma=False, grid=False, flat=False, balanced=False, out_dtype=None,
-                 test_timeout=False, stream=None):
+                 test_timeout=False, host_io=False, stream=None):
     """Attention of each request's query block over its paged keys.
 
     q [B, sq, Hq, D]; kv_cache [num_pages, Hkv, P, 2*D] (bf16, fp16, or uint8 /
     float8_e4m3fn for fp8, with q of the same type); block_table int32 [B, W];
     seq_lens int32 [B].  Returns (out [B, sq, Hq, D], lse fp32 [B, sq, Hq]).
     max_kv_len defaults to the table's capacity W * P (no host sync).
-    test_timeout sets the diagnostic PKD_FLAG_TEST_TIMEOUT.
+    test_timeout sets the diagnostic PKD_FLAG_TEST_TIMEOUT.  host_io sets
+    PKD_FLAG_HOST_IO: q, block_table, seq_lens (and out, lse, allocated pinned
+    when not given) are pinned host tensors that the kernels read and write in
+    place; kv_cache and the workspace stay on the device.
     """
     lib = load_library()
-    for t, n in ((q, "q"), (kv_cache, "kv_cache"), (block_table, "block_table"), (seq_lens, "seq_lens")):
-        _cuda(t, n)
+    _cuda(kv_cache, "kv_cache")
+    io = ((q, "q"), (block_table, "block_table"), (seq_lens, "seq_lens"), (out, "out"), (lse, "lse"))
+    for t, n in io:
+        if host_io:
+            if t is not None and (t.is_cuda or not t.is_pinned()):
+                raise ValueError(f"{n} must be a pinned host tensor with host_io")
+        else:
+            _cuda(t, n)
     B, sq, Hq, D = q.shape
     num_pages, Hkv, P, twoD = kv_cache.shape
     if twoD != 2 * D:
@@ -189,19 +199,21 @@ def paged_decode(q, kv_cache, block_table, seq_lens, scale, window=0, out=None, 
         raise ValueError("block_table rows must be contiguous")
     kv_dt = dtype_code(kv_cache.dtype)
     q_dt = dtype_code(q.dtype)
+    place = dict(pin_memory=True) if host_io else dict(device=q.device)
     if out is None:
         odt = out_dtype or (torch.bfloat16 if kv_dt == FP8_E4M3 else q.dtype)
-        out = torch.empty((B, sq, Hq, D), dtype=odt, device=q.device)
+        out = torch.empty((B, sq, Hq, D), dtype=odt, **place)
     if lse is None:
-        lse = torch.empty((B, sq, Hq), dtype=torch.float32, device=q.device)
+        lse = torch.empty((B, sq, Hq), dtype=torch.float32, **place)
     if max_kv_len is None:
         max_kv_len = block_table.shape[1] * P
     flags = (FLAG_CAUSAL if causal else 0) | (FLAG_MMA_SMALL_M if mma_small_m else 0) | \
         (FLAG_FMA if force_fma else 0) | (FLAG_GRID if grid else 0) | (FLAG_FLAT if flat else 0) | \
-        (FLAG_BALANCED if balanced else 0) | (FLAG_TEST_TIMEOUT if test_timeout else 0)
+        (FLAG_BALANCED if balanced else 0) | (FLAG_TEST_TIMEOUT if test_timeout else 0) | \
+        (FLAG_HOST_IO if host_io else 0)
     need = workspace_size(B, sq, Hq, Hkv, D, P, max_kv_len, kv_dt, window, chunk_tokens, flags)
     if workspace is None:
-        workspace = _workspace(need, q.device)
+        workspace = _workspace(need, kv_cache.device)
     _check(lib.pkd_paged_decode(
         _ptr(q), q_dt, _ptr(kv_cache), kv_dt, num_pages, _ptr(block_table), block_table.stride(0), _ptr(seq_lens),
         B, sq, Hq, Hkv, D, P, int(max_kv_len), float(scale), float(q_scale), float(k_scale), float(v_scale),

@@ -98,7 +98,8 @@ pkd_status make_plan(int B, int sq, int Hq, int Hkv, int D, int P, int max_kv_le
     // 16-bit query blocks of 17-32 rows, dense or causal: the tcgen05 kernel
     // (query_block_sq8: see the kernel-choice table of the design notes)
     pl.tc = !pl.bal && !pl.flat && (kv == PKD_BF16 || kv == PKD_FP16) && D == 128 && sq * (Hq / Hkv) > 16 &&
-            sq * (Hq / Hkv) <= 32 && B <= pkd::kTcMaxBatch && !(flags & (PKD_FLAG_GRID | PKD_FLAG_FMA)) &&
+            sq * (Hq / Hkv) <= 32 && B <= pkd::kTcMaxBatch &&
+            !(flags & (PKD_FLAG_GRID | PKD_FLAG_FMA | PKD_FLAG_HOST_IO)) &&
             (chunk_tokens <= 0 || chunk_tokens <= pkd::kTcMaxChunk);
     if (kv == PKD_FP8_E4M3 && (flags & PKD_FLAG_FMA)) {
         if (M > 8) return fail(PKD_EUNSUPPORTED, "fp8 on CUDA cores supports sq*num_heads/num_kv_heads <= 8 (got %d)", M);
@@ -430,6 +431,18 @@ pkd_status pkd_workspace_check(void* workspace, size_t workspace_bytes, void* st
                                     "entry outside [0, num_pages); those keys were skipped");
 }
 
+// Host memory registered with CUDA (pinned) whose device address, under
+// unified addressing, is the host address itself.
+static bool mapped_host(const void* ptr) {
+    cudaPointerAttributes a;
+    std::memset(&a, 0, sizeof a);
+    if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeHost && a.devicePointer == ptr;
+}
+
 pkd_status pkd_paged_decode(const void* q, pkd_dtype q_dtype, const void* kv_cache, pkd_dtype kv_dtype,
                             int64_t num_pages, const int32_t* block_table, int64_t block_table_stride,
                             const int32_t* seq_lens, int batch, int sq, int num_heads, int num_kv_heads,
@@ -451,6 +464,14 @@ pkd_status pkd_paged_decode(const void* q, pkd_dtype q_dtype, const void* kv_cac
     if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) || !aligned(workspace, 256) ||
         (lse && !aligned(lse, 4)) || !aligned(block_table, 4) || !aligned(seq_lens, 4))
         return fail(PKD_EINVAL, "misaligned pointer (q, kv_cache, out: 16 B; workspace: 256 B)");
+    if (flags & PKD_FLAG_HOST_IO) {
+        const void* io[5] = {q, block_table, seq_lens, out, lse};
+        static const char* const names[5] = {"q", "block_table", "seq_lens", "out", "lse"};
+        for (int i = 0; i < 5; ++i)
+            if (io[i] && !mapped_host(io[i]))
+                return fail(PKD_EINVAL, "PKD_FLAG_HOST_IO: %s is not pinned host memory mapped at its own address",
+                            names[i]);
+    }
     if (num_pages < 1) return fail(PKD_EINVAL, "num_pages must be >= 1");
     if ((int64_t)num_pages * num_kv_heads * page_size >= (int64_t)1 << 31)
         return fail(PKD_EUNSUPPORTED, "cache too large: num_pages*num_kv_heads*page_size must be < 2^31");

@@ -121,6 +121,25 @@ def test_null_pointers_are_einval(lib):
     assert b"null" in lib.pkd_last_error()
 
 
+def test_host_io_refuses_memory_not_registered_with_cuda(lib):
+    # plain host buffers: refused by the pointer check, before any CUDA work
+    bufs = [ctypes.create_string_buffer(1 << 16) for _ in range(6)]
+    a = [ctypes.c_void_p((ctypes.addressof(b) + 255) // 256 * 256) for b in bufs]
+    st = _decode_call(lib, q=a[0], kv=a[1], bt=a[2], lens=a[3], out=a[4], ws=a[5], flags=pkd.FLAG_HOST_IO)
+    assert st == pkd.EINVAL
+    assert b"PKD_FLAG_HOST_IO: q is not pinned host memory" in lib.pkd_last_error()
+
+
+def test_host_io_plans_run_the_chunked_grid_for_tcgen05_shapes(lib):
+    shape = (50, 8, 32, 8, 128, 16, 2048, pkd.BF16)
+    assert pkd.FLAG_HOST_IO == 128
+    assert pkd.kernel_name(*shape) == "persistent tcgen05 kernel, TMEM accumulators"
+    assert pkd.kernel_name(*shape, flags=pkd.FLAG_HOST_IO) == pkd.kernel_name(*shape, flags=pkd.FLAG_GRID)
+    assert pkd.workspace_size(*shape, flags=pkd.FLAG_HOST_IO) == pkd.workspace_size(*shape, flags=pkd.FLAG_GRID)
+    assert pkd.kernel_name(64, 1, 32, 8, 128, 16, 4096, pkd.BF16, flags=pkd.FLAG_HOST_IO) == \
+        pkd.kernel_name(64, 1, 32, 8, 128, 16, 4096, pkd.BF16)
+
+
 def test_mismatched_q_and_cache_types(lib):
     assert _decode_call(lib, q_dt=pkd.FP16) == pkd.EUNSUPPORTED
 
