@@ -138,9 +138,6 @@ struct MmaWarp {
                 for (int c = 0; c < 4; ++c) oacc[dt][n][c] = 0.f;
     }
 
-    // Fold one stage into the state.  Logits are scale2 * q.k + bias2 (log2
-    // domain); key kt (0..15) is used by row `row` iff kt < nvalid and
-    // visible(row, kt).  V rows at or past nvalid must be finite (zeroed).
     // Row half h of row tile mt feeds P.V n-tile 2*mt + h; halves past NT
     // hold only padding rows and are skipped.
     static __device__ __forceinline__ constexpr bool half_used(int mt, int h) { return 2 * mt + h < NT; }
@@ -148,24 +145,32 @@ struct MmaWarp {
     // Fold one stage into the state.  Logits are scale2 * q.k + bias2 (log2
     // domain).  kMasked: key kt (0..15) is used by row `row` iff kt < nvalid
     // and visible(row, kt), and V rows at or past nvalid must be finite
-    // (zeroed); otherwise all 16 keys are used by every row.
-    template <bool kMasked, class Visible>
+    // (zeroed); otherwise all 16 keys are used by every row.  kSplitQK: see qk.
+    template <bool kMasked, bool kSplitQK = false, class Visible>
     __device__ __forceinline__ void consume(uint32_t st, int half, int nvalid, float scale2, float bias2,
                                             Visible visible, int lane) {
         float sacc[MT][2][4];
-        qk(st, sacc, lane);
+        qk<kSplitQK>(st, sacc, lane);
         softmax_pv<kMasked>(sacc, st + half, nvalid, scale2, bias2, visible, lane);
     }
 
-    // S = Q K^T for the 16 keys of the K tile at `st`.
+    // S = Q K^T for the 16 keys of the K tile at `st`.  kSplit (one row tile
+    // only): the k-steps accumulate in two chains, even and odd, summed at the
+    // end, which halves the dependent MMA chain of a stage.  It pays where a
+    // warp's wait-to-refill chain per stage is the limit (segments: 66.5 ->
+    // 65.9 us on dash_paged_n256); elsewhere it gains nothing and its
+    // registers spill.
+    template <bool kSplit = false>
     __device__ __forceinline__ void qk(uint32_t st, float (&sacc)[MT][2][4], int lane) const {
+        static_assert(!kSplit || MT == 1, "two chains for one row tile only");
         const int mi = lane >> 3, ri = lane & 7;
+        float sodd[MT][2][4];
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
             for (int n = 0; n < 2; ++n)
 #pragma unroll
-                for (int c = 0; c < 4; ++c) sacc[mt][n][c] = 0.f;
+                for (int c = 0; c < 4; ++c) sacc[mt][n][c] = sodd[mt][n][c] = 0.f;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
             uint32_t b00, b01, b10, b11;
@@ -174,10 +179,16 @@ struct MmaWarp {
             for (int mt = 0; mt < MT; ++mt) {
                 uint32_t a[4];
                 q_frag(mt, kk, a, lane);
-                mma16816<kBF16>(sacc[mt][0], a, b00, b01);
-                mma16816<kBF16>(sacc[mt][1], a, b10, b11);
+                float (&acc)[2][4] = (kSplit && (kk & 1)) ? sodd[mt] : sacc[mt];
+                mma16816<kBF16>(acc[0], a, b00, b01);
+                mma16816<kBF16>(acc[1], a, b10, b11);
             }
         }
+        if constexpr (kSplit)
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) sacc[0][n][c] += sodd[0][n][c];
     }
 
     // Head dim of accumulator element c of d-tile dt held by lane group g.

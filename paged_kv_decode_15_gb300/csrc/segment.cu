@@ -369,8 +369,15 @@ segmented_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         // (masked keys weigh 0, and 0 * NaN is not 0); a partial stage's rows
         // outside the segment were zero-filled by its copies
         if (nvalid == 0) zero_tail_v<D, 2>(ring_gen + buf * S::STAGE, 0, lane);
-        wp.consume(st, S::HALF, nvalid, nvalid < kStageTok || lo > 0, p.scale_log2, kSegOut ? 0.f : sb[g],
-                   [&](int row, int kt) { return row < M && kt >= lo; }, lane);
+        {
+            // Q.K^T in two accumulation chains (kSplitQK)
+            const float bias2 = kSegOut ? 0.f : sb[g];
+            auto visible = [&](int row, int kt) { return row < M && kt >= lo; };
+            if (nvalid < kStageTok || lo > 0)
+                wp.template consume<true, true>(st, S::HALF, nvalid, p.scale_log2, bias2, visible, lane);
+            else
+                wp.template consume<false, true>(st, S::HALF, nvalid, p.scale_log2, bias2, visible, lane);
+        }
         __syncwarp();
         if (k + kSegNbuf < my_n) {
             fence_proxy_async();
